@@ -1,0 +1,217 @@
+/*
+ * dd.h -- C ABI of libdd.so: the predictive sparse-KV decode step on one GB300
+ * (sm_103a).
+ *
+ * The operation is the one the DualDecoder paper ("DualDecoder: Accelerate
+ * Long Context LLM Inference by Predictive Prefetch", arXiv:2607.26475)
+ * describes.  For each layer and each (request b, KV head h_kv), the library:
+ *   1. scores the speculated token's query against the key cache,
+ *      alpha = softmax(q_spec K^T / sqrt(d_k))
+ *      (summary page of the paper, "core formulas"; paper Sec. 1: the
+ *      retrieval index is computed from the token being processed);
+ *   2. selects the per-head top-k entries, I = argtopk(alpha, k)
+ *      (same formula; paper Fig. 1 "Select Top-k");
+ *   3. gathers only the selected K/V rows from a pinned host-memory KV store
+ *      into a layer-scoped GPU buffer (paper Sec. 2.2 and Fig. 1 "Sparse KV
+ *      Gather"; summary page worked example, step 5);
+ *   4. runs decode attention for the real query over the gathered rows plus a
+ *      local window of the most recent W positions (paper Fig. 1 "Attention");
+ *   5. loops over layers on two streams so that the gather of layer l+1
+ *      overlaps the attention of layer l, through a double-buffered scratch
+ *      region of O(k*d) bytes (paper Sec. 1: layer-aware transfer schedule and
+ *      layer-scoped memory manager; summary page, memory formula O(n*d) ->
+ *      O(k*d)).
+ *
+ * Conventions (every call):
+ *  - Element type: DD_F32 (IEEE binary32) or DD_BF16 (bfloat16) for q_spec, q,
+ *    K and V; all arithmetic accumulates in fp32; outputs are fp32.
+ *  - Layouts are dense row-major, units are (b, h_kv) with u = b*H_kv + h_kv:
+ *      q_spec, q        [B][H_q][d]
+ *      K (device)       [B][H_kv][n][d]     the layer's full key cache in HBM
+ *      K, V (host)      [B][H_kv][n][d]     pinned host store of the layer
+ *      V window         [B][H_kv][W][d]     device copy of V rows [n-W, n)
+ *      idx              [B][H_kv][k] int32  ascending positions in [0, n-W)
+ *      sel_score        [B][H_kv][k] fp32   alpha (MHA) or group sum of alpha
+ *      lse              [B][H_q]     fp32   log sum_j exp(s_j) over all n
+ *      k_buf, v_buf     [B][H_kv][k][d]     gathered rows, in idx order
+ *      out              [B][H_q][d]  fp32
+ *    Query head h uses KV head h / (H_q / H_kv) (grouped-query attention).
+ *  - Supported: head_dim 64 or 128 (fp32) and 64, 128 or 256 (bf16);
+ *    H_q % H_kv == 0; 1 <= k <= n - W; 0 <= W < n.  Other shapes return
+ *    DD_ERR_UNSUPPORTED or DD_ERR_INVALID_ARG.
+ *  - Device pointers must be 16-byte aligned; host KV pointers must come from
+ *    cudaHostAlloc / cudaMallocHost / cudaHostRegister (page-locked, mapped
+ *    under unified addressing); pageable host memory is rejected.
+ *  - Ownership: the caller owns every buffer passed in; the library never
+ *    frees or retains them.  A dd_ctx owns only its scratch slots, its
+ *    workspace and its events.
+ *  - Synchronisation: calls enqueue work on the given stream(s) and return
+ *    without synchronising.  Argument errors are reported synchronously
+ *    (nothing is enqueued); a launch failure returns DD_ERR_CUDA; faults
+ *    during execution surface at the caller's next synchronisation.
+ *  - No exceptions cross this boundary.  The library has no CPU fallback.
+ */
+#ifndef DD_H
+#define DD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DD_OK = 0,
+  DD_ERR_INVALID_ARG = 1, /* null/misaligned/pageable pointer, inconsistent sizes */
+  DD_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set */
+  DD_ERR_OOM = 3,         /* device allocation failed (dd_ctx_create only) */
+  DD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
+  DD_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait gave up */
+} dd_status;
+
+typedef enum { DD_F32 = 0, DD_BF16 = 1 } dd_dtype;
+
+/* One layer's shape. */
+typedef struct {
+  int32_t batch;      /* B: concurrent requests */
+  int32_t n_q_heads;  /* H_q */
+  int32_t n_kv_heads; /* H_kv (divides H_q) */
+  int32_t head_dim;   /* d */
+  int32_t ctx_len;    /* n: cached positions */
+  int32_t top_k;      /* k: rows selected per (request, KV head) */
+  int32_t window;     /* W: most recent positions always attended */
+  int32_t dtype;      /* dd_dtype of q_spec, q, K, V */
+} dd_shape;
+
+/* Same handle type as cudaStream_t. */
+typedef struct CUstream_st* dd_stream_t;
+
+/* Static description of a status code; never NULL. */
+const char* dd_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int dd_version(void);
+
+/*
+ * Bytes of device workspace that dd_score_topk and dd_sparse_decode_attn need
+ * for this shape (fp32 logits [B][H_q][round_up(n,4)], per-chunk softmax
+ * partials and split-k attention partials, each 256-byte aligned).
+ * The two calls use disjoint parts, so one buffer serves both.
+ * Returns DD_ERR_INVALID_ARG / DD_ERR_UNSUPPORTED for bad shapes.
+ */
+dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes);
+
+/*
+ * Steps 1-2 for one layer: logits s[b,h,j] = q_spec[b,h] . K[b,h_kv(h),j] /
+ * sqrt(d) for all j < n; lse_out[b,h] = log sum_j exp(s[b,h,j]); selection
+ * score a[j] = exp(s_j - lse) (MHA) or sum over the query heads of the group
+ * of exp(s_hj - lse_h) (GQA); idx_out = the k positions of [0, n-W) with the
+ * largest a, ties to the lower position, written in ascending order, and
+ * sel_score_out = a at those positions.
+ *   q_spec   device [B][H_q][d]            k_dev  device [B][H_kv][n][d]
+ *   idx_out  device [B][H_kv][k] int32     sel_score_out device [B][H_kv][k]
+ *   lse_out  device [B][H_q] fp32 (may be NULL)
+ *   workspace device, at least dd_workspace_size bytes.
+ */
+dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k_dev,
+                        int32_t* idx_out, float* sel_score_out, float* lse_out, void* workspace,
+                        size_t ws_bytes, dd_stream_t stream);
+
+/*
+ * Step 3 for one layer: for every unit u and slot i < k, copy row
+ * idx[u][i] of the pinned host K and V stores into row i of k_buf / v_buf.
+ * The rows are read by the GPU directly from page-locked host memory
+ * (zero-copy loads through unified addressing, over the host link).
+ *   k_host, v_host  pinned host [B][H_kv][n][d]
+ *   idx             device [B][H_kv][k] int32, each in [0, n) (not checked
+ *                   on the device: an out-of-range index reads outside the
+ *                   store; dd_score_topk only produces in-range indices)
+ *   k_buf, v_buf    device [B][H_kv][k][d]
+ *   mode            0 = zero-copy gather kernel (the only mode; others
+ *                   return DD_ERR_UNSUPPORTED)
+ */
+dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v_host,
+                        const int32_t* idx, void* k_buf, void* v_buf, int mode,
+                        dd_stream_t stream);
+
+/*
+ * Step 4 for one layer: out[b,h] = sum_{j in S} softmax_S(q[b,h] . K_j /
+ * sqrt(d)) V_j with S = the k gathered rows followed by the W window rows
+ * [n-W, n).  Gathered rows come from k_buf / v_buf, window keys from k_dev
+ * (rows [n-W, n) of each unit) and window values from v_win.  Split-k over
+ * the k+W rows with a log-sum-exp merge of the partials (in workspace).
+ *   q      device [B][H_q][d]        k_buf, v_buf device [B][H_kv][k][d]
+ *   k_dev  device [B][H_kv][n][d]    v_win device [B][H_kv][W][d] (NULL if W=0)
+ *   out    device [B][H_q][d] fp32
+ */
+dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void* k_buf,
+                                const void* v_buf, const void* k_dev, const void* v_win,
+                                float* out, void* workspace, size_t ws_bytes,
+                                dd_stream_t stream);
+
+/* ---------------------------- layer loop ---------------------------- */
+
+typedef struct dd_ctx dd_ctx;
+
+/* Per-layer inputs and output of dd_decode_step (pointers as above). */
+typedef struct {
+  const void* q_spec; /* device [B][H_q][d] */
+  const void* q;      /* device [B][H_q][d] */
+  const void* k_dev;  /* device [B][H_kv][n][d] */
+  const void* k_host; /* pinned host [B][H_kv][n][d] */
+  const void* v_host; /* pinned host [B][H_kv][n][d] */
+  const void* v_win;  /* device [B][H_kv][W][d] (NULL if W = 0) */
+  float* out;         /* device [B][H_q][d] */
+} dd_layer_io;
+
+/*
+ * Allocate the layer-scoped state for one shape: two scratch slots of
+ * gathered K/V rows (2 x 2 x B*H_kv*k*d elements; independent of n), two index
+ * slots, the workspace and the events.  Returns DD_ERR_OOM on allocation
+ * failure.  Uses the current CUDA device; the context is bound to it.
+ */
+dd_status dd_ctx_create(const dd_shape* shape, dd_ctx** out);
+void dd_ctx_destroy(dd_ctx* ctx);
+
+/* Bytes of device memory a context holds (scratch slots + workspace). */
+size_t dd_ctx_device_bytes(const dd_ctx* ctx);
+
+enum {
+  DD_STEP_TIMING = 1 /* record per-phase CUDA events; read with dd_ctx_timings */
+};
+
+/*
+ * Enqueue one decode step over n_layers layers.  Steps 1-2 of layer l+1 run
+ * on `compute` ahead of the attention of layer l; the gather of layer l+1 runs
+ * on `copy` into the other scratch slot while layer l's attention runs.
+ * Events order each gather after its indices and after the attention that
+ * last read its slot, and each attention after its gather.  The copy stream
+ * is joined back into `compute` before return.  If copy == compute (or copy
+ * is NULL) every phase runs in order on `compute` (the serial schedule, with
+ * bit-identical results).
+ */
+dd_status dd_decode_step(dd_ctx* ctx, const dd_layer_io* layers, int n_layers,
+                         dd_stream_t compute, dd_stream_t copy, int flags);
+
+/* Phase times of the last dd_decode_step run with DD_STEP_TIMING, in ms. */
+typedef struct {
+  float step_ms;      /* first event to last event on `compute` */
+  float score_ms;     /* sum over layers of the scoring kernel */
+  float topk_ms;      /* sum over layers of LSE merge + top-k */
+  float gather_ms;    /* sum over layers of the gather */
+  float attn_ms;      /* sum over layers of attention (+ merge) */
+  int32_t n_layers;
+  int32_t launches;   /* kernels launched by that step */
+} dd_phase_times;
+
+/* Wait for the last timed step and read its phase times. */
+dd_status dd_ctx_timings(dd_ctx* ctx, dd_phase_times* out);
+
+/* Per-layer scoring-kernel times (ms) of the last timed step; n entries max. */
+dd_status dd_ctx_score_times(dd_ctx* ctx, float* out_ms, int n);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DD_H */
