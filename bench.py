@@ -1,0 +1,407 @@
+"""Benchmark of the predictive sparse-KV decode step on one GB300.
+
+A step is one dd_decode_step over all L layers of the LLaMA-2-7B-shaped
+workload (32 layers cycling 8 distinct layer slots, batch 8, 32 MHA heads x
+128, context 32768, top-k 128 + a 64-token window, bf16): scoring, top-k,
+gather from pinned host memory and attention for every layer, on two streams.
+
+Prints one JSON line: layer-steps/s (device time, inputs resident), the same
+through the public API with host copies (e2e), the scoring kernel's HBM
+roofline, the gather's host-link bandwidth against a pinned-copy probe taken in
+the same process, the hidden fraction of the gather, and the fp64 oracle timed
+on the host cores as the CPU baseline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME] [--profile-case]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "sparse-decode layer-steps/s; scoring HBM GB/s; gather host-link GB/s"
+UNIT = "layer-steps/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--workload", default=synth.C2.name, choices=list(synth.WORKLOADS))
+    p.add_argument("--profile-case", action="store_true",
+                   help="small case for ncu captures: batch 2, 2 layers, 1 slot")
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="CPU work budget of the oracle baseline")
+    return p.parse_args()
+
+
+def workload(args):
+    w = synth.WORKLOADS[args.workload]
+    if args.profile_case:
+        w = w.scaled(batch=2, n_layers=2, n_slots=1)
+    return w
+
+
+# --------------------------------------------------------------- distributed
+
+def dist_init(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def measured_hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        v = float(json.load(open(p))["hbm_gbs"])
+        return v, "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------- CPU baseline
+
+def oracle_layer_rate(w, host, seconds: float, max_layers: int | None = None):
+    """Time the fp64 oracle (all steps) on whole layers of slot 0, using every
+    host core, for about `seconds` (or max_layers layers).  Returns
+    (layer-steps/s, cores, layers timed)."""
+    import oracle
+    cores = os.cpu_count() or 1
+    os_ = oracle.Shape(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.ctx_len, w.top_k,
+                       w.window, w.dtype)
+    orc = oracle.get()
+    t0 = time.perf_counter()
+    layers = 0
+    while True:
+        orc.layer(os_, host["q_spec"], host["q"], host["K"], host["V"], nthreads=cores)
+        layers += 1
+        el = time.perf_counter() - t0
+        if (max_layers and layers >= max_layers) or (not max_layers and el >= seconds):
+            break
+    return layers / el, cores, layers
+
+
+def host_slot(w, slot=0):
+    """One layer slot on the host (plain memory) for the oracle."""
+    dt = np.uint16 if w.dtype == synth.BF16 else np.float32
+    q_spec = np.empty((w.batch, w.n_q_heads, w.head_dim), dt)
+    q = np.empty_like(q_spec)
+    K = np.empty((w.batch, w.n_kv_heads, w.ctx_len, w.head_dim), dt)
+    V = np.empty_like(K)
+    synth.fill_slot(w, slot, q_spec, q, K, V)
+    return {"q_spec": q_spec, "q": q, "K": K, "V": V}
+
+
+def config_of(w, args):
+    return {"workload": w.name, "layers": w.n_layers, "distinct_layer_slots": w.n_slots,
+            "batch": w.batch, "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "ctx_len": w.ctx_len, "top_k": w.top_k, "window": w.window,
+            "l2": "inputs larger than L2 (K of one layer is %.0f MiB; 129 MB L2)"
+                  % (w.k_bytes() / 2**20),
+            "parallelism": f"replicas x{args.gpus} (independent requests per GPU)"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: each step is one whole layer of slot 0."""
+    if rank != 0:
+        return
+    w = workload(args)
+    host = host_slot(w)
+    cores = os.cpu_count() or 1
+    oracle_layer_rate(w, host, 0, max_layers=max(1, args.warmup))
+    rate, cores, layers = oracle_layer_rate(w, host, 0, max_layers=max(1, args.steps))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 / rate, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w, args),
+        "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{layers} whole layers of layer slot 0 (all "
+                                   f"{w.units} (request, KV head) units), fp64 C oracle"},
+        "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world):
+    import sparse_kv_prefetch_gb300 as dd
+
+    w = workload(args)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    dt = torch.bfloat16 if w.dtype == synth.BF16 else torch.float32
+    B, Hq, Hkv, d, n, k, W = (w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.ctx_len,
+                              w.top_k, w.window)
+    D, L = w.n_slots, w.n_layers
+
+    # Host store (pinned) and the device-resident key cache, per layer slot.
+    K_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
+    V_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
+    qs_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
+    q_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
+    t_gen = time.perf_counter()
+    for s in range(D):
+        synth.fill_slot(w, s, qs_h[s], q_h[s], K_h[s], V_h[s])
+    t_gen = time.perf_counter() - t_gen
+    K_d = K_h.to(dev)
+    qs_d, q_d = qs_h.to(dev), q_h.to(dev)
+    vwin_d = V_h[:, :, :, n - W:, :].contiguous().to(dev) if W > 0 else None
+    outs = torch.empty((L, B, Hq, d), dtype=torch.float32, device=dev)
+
+    shape = dd.Shape(B, Hq, Hkv, d, n, k, W, w.dtype)
+    ctx = dd.Ctx(shape)
+    compute = torch.cuda.Stream()
+    copy = torch.cuda.Stream(priority=-1)
+    layers = dd.Ctx.pack([dd.LayerIO(qs_d[l % D], q_d[l % D], K_d[l % D], K_h[l % D],
+                                     V_h[l % D], vwin_d[l % D] if W > 0 else None, outs[l])
+                          for l in range(L)])
+    torch.cuda.synchronize()
+
+    # Host-link probe: one large contiguous pinned H2D copy, median of 10.
+    probe_bytes = min(1 << 30, K_h[0].numel() * K_h.element_size())
+    src = K_h[0].view(-1).view(torch.uint8)[:probe_bytes]
+    dst = torch.empty(probe_bytes, dtype=torch.uint8, device=dev)
+    probe = []
+    for i in range(13):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        dst.copy_(src, non_blocking=True)
+        e1.record()
+        e1.synchronize()
+        if i >= 3:
+            probe.append(probe_bytes / (e0.elapsed_time(e1) * 1e-3) / 1e9)
+    probe_gbs = statistics.median(probe)
+    del dst
+
+    def step(copy_stream, timing=True):
+        ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing)
+        return ctx.timings() if timing else None
+
+    compute.wait_stream(torch.cuda.current_stream())
+    for _ in range(max(3, args.warmup)):
+        step(copy)
+    torch.cuda.synchronize()
+
+    # Timed region: K overlapped steps, device time on the compute stream.
+    clocks = ClockSampler(dev.index)
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(compute)
+    phases, score_ms, launches = [], [], 0
+    for _ in range(args.steps):
+        t = step(copy)
+        phases.append(t)
+        score_ms.extend(ctx.score_times(L))
+        launches += t["launches"]
+    ev1.record(compute)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_s = ev0.elapsed_time(ev1) * 1e-3
+    total_s = max_over_ranks(total_s, world)
+    value = world * L * args.steps / total_s
+
+    # Serial schedule (same work, one stream) for the hidden fraction.
+    serial = [step(None) for _ in range(max(3, args.steps // 4))]
+    torch.cuda.synchronize()
+
+    # End to end through the public API: per step copy every layer's q_spec and q
+    # from pinned host memory, run the step, read every layer's output back.
+    out_h = torch.empty((L, B, Hq, d), dtype=torch.float32, pin_memory=True)
+    qs_l = torch.empty((L, B, Hq, d), dtype=dt, device=dev)
+    q_l = torch.empty((L, B, Hq, d), dtype=dt, device=dev)
+    qs_src = torch.stack([qs_h[l % D] for l in range(L)]).pin_memory()
+    q_src = torch.stack([q_h[l % D] for l in range(L)]).pin_memory()
+    layers_e2e = dd.Ctx.pack([dd.LayerIO(qs_l[l], q_l[l], K_d[l % D], K_h[l % D], V_h[l % D],
+                                         vwin_d[l % D] if W > 0 else None, outs[l])
+                              for l in range(L)])
+    e2e_steps = max(3, args.steps // 2)
+
+    def e2e_step():
+        with torch.cuda.stream(compute):
+            qs_l.copy_(qs_src, non_blocking=True)
+            q_l.copy_(q_src, non_blocking=True)
+        ctx.decode_step(layers_e2e, compute=compute, copy=copy)
+        with torch.cuda.stream(compute):
+            out_h.copy_(outs, non_blocking=True)
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(compute)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(compute)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world)
+    e2e_value = world * L * e2e_steps / e2e_s
+    if not torch.equal(out_h.to(dev), outs):
+        raise RuntimeError("e2e read-back differs from the device outputs")
+
+    # Derived rates.
+    k_bytes, g_bytes = w.k_bytes(), w.gather_bytes()
+    score_mean_ms = statistics.mean(score_ms)
+    score_gbs = k_bytes / (score_mean_ms * 1e-3) / 1e9
+    gather_ms_layer = statistics.mean(p["gather_ms"] for p in phases) / L
+    gather_gbs = g_bytes / (gather_ms_layer * 1e-3) / 1e9
+    t_over = statistics.median(p["step_ms"] for p in phases)
+    t_ser = statistics.median(p["step_ms"] for p in serial)
+    g_ser = statistics.median(p["gather_ms"] for p in serial)
+    comp_ser = statistics.median(p["score_ms"] + p["topk_ms"] + p["attn_ms"] for p in serial)
+    hidden = max(0.0, min(1.0, (t_ser - t_over) / g_ser)) if g_ser > 0 else None
+    peak, peak_kind = measured_hbm_peak()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.profile_case:
+        host = {"q_spec": qs_h[0], "q": q_h[0], "K": K_h[0], "V": V_h[0]}
+        rate, cores, nl = oracle_layer_rate(w, host, args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{nl} whole layers of layer slot 0 (all {w.units} (request, KV head) "
+                         f"units: scoring, full-sort top-k, attention) in fp64, "
+                         f"~{args.cpu_seconds:.0f} s"}
+
+    if rank != 0:
+        ctx.close()
+        return
+    elt = 2 if w.dtype == synth.BF16 else 4
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": total_s * 1e3 / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.dtype == synth.BF16 else "f32",
+        "data": "synthetic: seeded SplitMix64/Box-Muller K, V, q_spec ~ N(0,1), planted keys, "
+                "q = q_spec + N(0, 0.1^2)",
+        "config": config_of(w, args),
+        "scoring_hbm_gbs": score_gbs,
+        "gather_host_link_gbs": gather_gbs,
+        "host_link_probe_gbs": probe_gbs,
+        "gather_frac_of_probe": gather_gbs / probe_gbs,
+        "hidden_fraction": hidden,
+        "hidden_bound": min(1.0, comp_ser / g_ser) if g_ser > 0 else None,
+        "phase_ms_per_step": {kk: statistics.mean(p[kk] for p in phases)
+                              for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms", "attn_ms")},
+        "serial_step_ms": t_ser,
+        "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": score_gbs / peak, "traffic": None,
+                     "algorithmic_bytes_per_launch": k_bytes},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT,
+                "h2d_bytes_per_step": 2 * L * B * Hq * d * elt,
+                "d2h_bytes_per_step": L * B * Hq * d * 4,
+                "gather_host_bytes_per_step": L * g_bytes},
+        "gpu_launches": launches,
+        "clocks": clk,
+        "setup_s": {"generate": t_gen},
+        "ctx_device_bytes": ctx.device_bytes,
+    }
+    ctx.close()
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world = dist_init(args)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

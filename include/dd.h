@@ -124,9 +124,9 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
  * The rows are read by the GPU directly from page-locked host memory
  * (zero-copy loads through unified addressing, over the host link).
  *   k_host, v_host  pinned host [B][H_kv][n][d]
- *   idx             device [B][H_kv][k] int32, each in [0, n) (not checked
- *                   on the device: an out-of-range index reads outside the
- *                   store; dd_score_topk only produces in-range indices)
+ *   idx             device [B][H_kv][k] int32, each in [0, n); an index
+ *                   outside that range is clamped into it on the device, so
+ *                   the kernel never reads outside the store
  *   k_buf, v_buf    device [B][H_kv][k][d]
  *   mode            0 = zero-copy gather kernel (the only mode; others
  *                   return DD_ERR_UNSUPPORTED)

@@ -1,0 +1,244 @@
+"""GB300-native predictive sparse-KV decode step (DualDecoder's hot path).
+
+Thin ctypes binding of ``libdd.so`` (declared in ``include/dd.h``): argument
+marshalling only, with the C names.  Every step runs in the library's CUDA
+kernels; there is no CPU fallback, and every call raises if the library has not
+been built (``python -m sparse_kv_prefetch_gb300.build``).
+
+Buffers are torch tensors (device tensors for device arguments, page-locked CPU
+tensors for the host KV store) or raw integer addresses.  Streams are
+``torch.cuda.Stream`` objects, raw ``cudaStream_t`` integers, or None for the
+current torch stream.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import NamedTuple, Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdd.so")
+
+DD_OK, DD_ERR_INVALID_ARG, DD_ERR_UNSUPPORTED, DD_ERR_OOM, DD_ERR_CUDA, DD_ERR_TIMEOUT = range(6)
+DD_F32, DD_BF16 = 0, 1
+DD_STEP_TIMING = 1
+
+
+class DDError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {_lib().dd_status_string(status).decode()} (status {status})")
+
+
+class dd_shape(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "n_q_heads", "n_kv_heads", "head_dim", "ctx_len", "top_k", "window", "dtype")]
+
+
+class dd_layer_io(ctypes.Structure):
+    _fields_ = [("q_spec", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k_dev", ctypes.c_void_p),
+                ("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p),
+                ("v_win", ctypes.c_void_p), ("out", ctypes.c_void_p)]
+
+
+class dd_phase_times(ctypes.Structure):
+    _fields_ = [("step_ms", ctypes.c_float), ("score_ms", ctypes.c_float),
+                ("topk_ms", ctypes.c_float), ("gather_ms", ctypes.c_float),
+                ("attn_ms", ctypes.c_float), ("n_layers", ctypes.c_int32),
+                ("launches", ctypes.c_int32)]
+
+
+@dataclass(frozen=True)
+class Shape:
+    """One layer: B, H_q, H_kv, d, n, k, W, dtype (DD_F32 or DD_BF16)."""
+    batch: int
+    n_q_heads: int
+    n_kv_heads: int
+    head_dim: int
+    ctx_len: int
+    top_k: int
+    window: int
+    dtype: int
+
+    def c(self) -> dd_shape:
+        return dd_shape(self.batch, self.n_q_heads, self.n_kv_heads, self.head_dim,
+                        self.ctx_len, self.top_k, self.window, self.dtype)
+
+
+_L = None
+
+
+def _lib():
+    global _L
+    if _L is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m sparse_kv_prefetch_gb300.build` (there is no fallback)")
+        L = ctypes.CDLL(LIB_PATH)
+        P, S = ctypes.c_void_p, ctypes.POINTER(dd_shape)
+        sig = {
+            "dd_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "dd_version": ([], ctypes.c_int),
+            "dd_workspace_size": ([S, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+            "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dd_gather_h2d": ([S, P, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
+            "dd_sparse_decode_attn": ([S, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dd_ctx_create": ([S, ctypes.POINTER(P)], ctypes.c_int),
+            "dd_ctx_destroy": ([P], None),
+            "dd_ctx_device_bytes": ([P], ctypes.c_size_t),
+            "dd_decode_step": ([P, ctypes.POINTER(dd_layer_io), ctypes.c_int, P, P, ctypes.c_int],
+                               ctypes.c_int),
+            "dd_ctx_timings": ([P, ctypes.POINTER(dd_phase_times)], ctypes.c_int),
+            "dd_ctx_score_times": ([P, ctypes.POINTER(ctypes.c_float), ctypes.c_int],
+                                   ctypes.c_int),
+        }
+        for name, (args, res) in sig.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _L = L
+    return _L
+
+
+def lib():
+    """The loaded libdd.so (ctypes.CDLL)."""
+    return _lib()
+
+
+def _check(status: int, what: str):
+    if status != DD_OK:
+        raise DDError(status, what)
+
+
+def _dev(x) -> Optional[int]:
+    """Address of a device buffer (CUDA tensor or raw int; None -> NULL)."""
+    if x is None or isinstance(x, int):
+        return x
+    if not x.is_cuda:
+        raise TypeError("expected a CUDA tensor")
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+def _host(x) -> Optional[int]:
+    """Address of a page-locked host buffer (pinned CPU tensor or raw int)."""
+    if x is None or isinstance(x, int):
+        return x
+    if x.is_cuda or not x.is_contiguous():
+        raise TypeError("expected a contiguous CPU tensor")
+    if not x.is_pinned():
+        raise ValueError("the host KV store must be page-locked (pin_memory=True)")
+    return x.data_ptr()
+
+
+def _stream(s) -> Optional[int]:
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def version() -> int:
+    return _lib().dd_version()
+
+
+def workspace_size(shape: Shape) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib().dd_workspace_size(ctypes.byref(shape.c()), ctypes.byref(n)), "dd_workspace_size")
+    return n.value
+
+
+def score_topk(shape: Shape, q_spec, k_dev, idx_out, sel_score_out, lse_out, workspace,
+               stream=None, ws_bytes: Optional[int] = None):
+    """Steps 1-2 (scoring + per-KV-head top-k) of one layer; see dd.h."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().dd_score_topk(ctypes.byref(shape.c()), _dev(q_spec), _dev(k_dev),
+                                _dev(idx_out), _dev(sel_score_out), _dev(lse_out),
+                                _dev(workspace), ws_bytes, _stream(stream)), "dd_score_topk")
+
+
+def gather_h2d(shape: Shape, k_host, v_host, idx, k_buf, v_buf, mode: int = 0, stream=None):
+    """Step 3: gather the selected K/V rows from pinned host memory; see dd.h."""
+    _check(_lib().dd_gather_h2d(ctypes.byref(shape.c()), _host(k_host), _host(v_host),
+                                _dev(idx), _dev(k_buf), _dev(v_buf), mode, _stream(stream)),
+           "dd_gather_h2d")
+
+
+def sparse_decode_attn(shape: Shape, q, k_buf, v_buf, k_dev, v_win, out, workspace, stream=None,
+                       ws_bytes: Optional[int] = None):
+    """Step 4: split-k attention over the gathered rows plus the window; see dd.h."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().dd_sparse_decode_attn(ctypes.byref(shape.c()), _dev(q), _dev(k_buf),
+                                        _dev(v_buf), _dev(k_dev), _dev(v_win), _dev(out),
+                                        _dev(workspace), ws_bytes, _stream(stream)),
+           "dd_sparse_decode_attn")
+
+
+class LayerIO(NamedTuple):
+    q_spec: object
+    q: object
+    k_dev: object
+    k_host: object
+    v_host: object
+    v_win: object
+    out: object
+
+
+class Ctx:
+    """Layer-scoped state (double-buffered scratch, workspace, events) for one shape."""
+
+    def __init__(self, shape: Shape):
+        self.shape = shape
+        h = ctypes.c_void_p()
+        _check(_lib().dd_ctx_create(ctypes.byref(shape.c()), ctypes.byref(h)), "dd_ctx_create")
+        self._h = h
+        self._keep = None
+
+    @property
+    def device_bytes(self) -> int:
+        return _lib().dd_ctx_device_bytes(self._h)
+
+    def close(self):
+        if self._h:
+            _lib().dd_ctx_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @staticmethod
+    def pack(layers: Sequence[LayerIO]):
+        """Marshal the per-layer buffers once (reuse across steps)."""
+        arr = (dd_layer_io * len(layers))()
+        for i, io in enumerate(layers):
+            arr[i] = dd_layer_io(_dev(io.q_spec), _dev(io.q), _dev(io.k_dev), _host(io.k_host),
+                                 _host(io.v_host), _dev(io.v_win), _dev(io.out))
+        return arr
+
+    def decode_step(self, layers, compute=None, copy=None, timing: bool = False):
+        """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
+        arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
+        cs = _stream(compute)
+        xs = None if copy is None else _stream(copy)
+        _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs,
+                                     DD_STEP_TIMING if timing else 0), "dd_decode_step")
+        self._keep = arr
+
+    def timings(self) -> dict:
+        t = dd_phase_times()
+        _check(_lib().dd_ctx_timings(self._h, ctypes.byref(t)), "dd_ctx_timings")
+        return {f: getattr(t, f) for f, _ in dd_phase_times._fields_}
+
+    def score_times(self, n: int):
+        buf = (ctypes.c_float * n)()
+        _check(_lib().dd_ctx_score_times(self._h, buf, n), "dd_ctx_score_times")
+        return list(buf)

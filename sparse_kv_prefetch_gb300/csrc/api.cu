@@ -1,0 +1,496 @@
+// C ABI of libdd.so: argument checks, workspace layout, the three per-layer
+// calls and the two-stream layer loop with its double-buffered, layer-scoped
+// scratch (DualDecoder paper Sec. 1: layer-aware transfer schedule and
+// layer-scoped KV memory manager; summary page: transfer time
+// T_transfer = sum_l S_l / B hidden by min max(T_compute, T_transfer), and the
+// runtime sparse-KV buffer reduced from O(n d) to O(k d)).
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <initializer_list>
+#include <new>
+#include <vector>
+
+#include "dd_internal.cuh"
+
+#define DD_VERSION 10000
+
+namespace dd {
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+int sm_count() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev < 64 && cached[dev]) return cached[dev];
+  int n = 1;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 1;
+  if (dev < 64) cached[dev] = n;
+  return n;
+}
+
+dd_status resolve(const dd_shape* s, Dims* o) {
+  if (!s || !o) return DD_ERR_INVALID_ARG;
+  if (s->batch < 1 || s->n_q_heads < 1 || s->n_kv_heads < 1 || s->head_dim < 1 ||
+      s->ctx_len < 1 || s->top_k < 1 || s->window < 0)
+    return DD_ERR_INVALID_ARG;
+  if (s->n_q_heads % s->n_kv_heads != 0) return DD_ERR_INVALID_ARG;
+  if (s->window >= s->ctx_len) return DD_ERR_INVALID_ARG;
+  if (s->top_k > s->ctx_len - s->window) return DD_ERR_INVALID_ARG;
+  if (s->dtype != DD_F32 && s->dtype != DD_BF16) return DD_ERR_UNSUPPORTED;
+  const int G = s->n_q_heads / s->n_kv_heads;
+  if (G != 1 && G != 2 && G != 4 && G != 8) return DD_ERR_UNSUPPORTED;
+  const int chunk = score_chunk(s->dtype, s->head_dim);
+  if (chunk == 0) return DD_ERR_UNSUPPORTED;
+  if (s->ctx_len > (1 << 30)) return DD_ERR_UNSUPPORTED;
+  Dims d;
+  d.B = s->batch;
+  d.Hq = s->n_q_heads;
+  d.Hkv = s->n_kv_heads;
+  d.G = G;
+  d.d = s->head_dim;
+  d.n = s->ctx_len;
+  d.k = s->top_k;
+  d.W = s->window;
+  d.dtype = s->dtype;
+  d.elt = s->dtype == DD_BF16 ? 2 : 4;
+  const long long U = (long long)d.B * d.Hkv;
+  if (U > (1 << 24)) return DD_ERR_UNSUPPORTED;
+  d.U = (int)U;
+  d.span = d.n - d.W;
+  d.ldn = (d.n + 3) & ~3;
+  d.chunk = chunk;
+  d.nchunks = (d.n + chunk - 1) / chunk;
+  if ((long long)d.U * d.nchunks > 0x7FFFFFFFLL) return DD_ERR_UNSUPPORTED;
+  d.rows = d.k + d.W;
+  d.nsplit = (d.rows + kAttnRowsPerSplit - 1) / kAttnRowsPerSplit;
+  if ((long long)d.U * d.k > 0x7FFFFFFFLL) return DD_ERR_UNSUPPORTED;
+  *o = d;
+  return DD_OK;
+}
+
+WsLayout ws_layout(const Dims& d) {
+  WsLayout w;
+  size_t off = 0;
+  w.logits = off;
+  off += align256((size_t)d.B * d.Hq * d.ldn * sizeof(float));
+  w.part = off;
+  off += align256((size_t)d.B * d.Hq * d.nchunks * sizeof(float2));
+  w.attn_o = off;
+  off += align256((size_t)d.B * d.Hq * d.nsplit * d.d * sizeof(float));
+  w.attn_ml = off;
+  off += align256((size_t)d.B * d.Hq * d.nsplit * sizeof(float2));
+  w.total = off;
+  return w;
+}
+
+}  // namespace dd
+
+using namespace dd;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+dd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DD_OK : DD_ERR_CUDA; }
+
+// True if p is device (or managed) memory of the current CUDA context.
+bool is_device_ptr(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+}
+
+bool all_device(std::initializer_list<const void*> ps) {
+  for (const void* p : ps)
+    if (p && !is_device_ptr(p)) return false;
+  return true;
+}
+
+// Device-accessible address of a page-locked host pointer; NULL if the
+// pointer is not page-locked host memory known to CUDA.
+const void* host_to_device(const void* p) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();  // clear the non-sticky error
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost) return nullptr;
+  return a.devicePointer;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dd_status_string(int s) {
+  switch (s) {
+    case DD_OK: return "ok";
+    case DD_ERR_INVALID_ARG: return "invalid argument";
+    case DD_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case DD_ERR_OOM: return "device allocation failed";
+    case DD_ERR_CUDA: return "CUDA runtime error";
+    case DD_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+int dd_version(void) { return DD_VERSION; }
+
+dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes) {
+  if (!bytes) return DD_ERR_INVALID_ARG;
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  *bytes = ws_layout(d).total;
+  return DD_OK;
+}
+
+dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k_dev,
+                        int32_t* idx_out, float* sel_score_out, float* lse_out, void* workspace,
+                        size_t ws_bytes, dd_stream_t stream) {
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  if (!q_spec || !k_dev || !idx_out || !sel_score_out || !workspace) return DD_ERR_INVALID_ARG;
+  if (!aligned16(q_spec) || !aligned16(k_dev) || !aligned16(workspace)) return DD_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  if (ws_bytes < w.total) return DD_ERR_INVALID_ARG;
+  if (!all_device({q_spec, k_dev, idx_out, sel_score_out, lse_out, workspace}))
+    return DD_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* logits = reinterpret_cast<float*>(ws + w.logits);
+  float2* part = reinterpret_cast<float2*>(ws + w.part);
+  st = cuda_status(launch_score(d, q_spec, k_dev, logits, part, s));
+  if (st != DD_OK) return st;
+  return cuda_status(launch_topk(d, logits, part, idx_out, sel_score_out, lse_out, s));
+}
+
+dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v_host,
+                        const int32_t* idx, void* k_buf, void* v_buf, int mode,
+                        dd_stream_t stream) {
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  if (mode != 0) return DD_ERR_UNSUPPORTED;
+  if (!k_host || !v_host || !idx || !k_buf || !v_buf) return DD_ERR_INVALID_ARG;
+  if (!aligned16(k_host) || !aligned16(v_host) || !aligned16(k_buf) || !aligned16(v_buf))
+    return DD_ERR_INVALID_ARG;
+  const void* kh = host_to_device(k_host);
+  const void* vh = host_to_device(v_host);
+  if (!kh || !vh) return DD_ERR_INVALID_ARG;
+  if (!all_device({idx, k_buf, v_buf})) return DD_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_gather(d, kh, vh, idx, k_buf, v_buf, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void* k_buf,
+                                const void* v_buf, const void* k_dev, const void* v_win,
+                                float* out, void* workspace, size_t ws_bytes,
+                                dd_stream_t stream) {
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  if (!q || !k_buf || !v_buf || !k_dev || !out || !workspace) return DD_ERR_INVALID_ARG;
+  if (d.W > 0 && !v_win) return DD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_buf) || !aligned16(v_buf) || !aligned16(k_dev) ||
+      !aligned16(out) || !aligned16(workspace) || (v_win && !aligned16(v_win)))
+    return DD_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  if (ws_bytes < w.total) return DD_ERR_INVALID_ARG;
+  if (!all_device({q, k_buf, v_buf, k_dev, v_win, out, workspace})) return DD_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  return cuda_status(launch_attn(d, q, k_buf, v_buf, k_dev, v_win, out,
+                                 reinterpret_cast<float*>(ws + w.attn_o),
+                                 reinterpret_cast<float2*>(ws + w.attn_ml),
+                                 reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"
+
+// ------------------------------------------------------------------ context
+
+enum Phase { PH_SCORE0, PH_SCORE1, PH_TOPK1, PH_GATHER0, PH_GATHER1, PH_ATTN0, PH_ATTN1, PH_N };
+
+struct dd_ctx {
+  dd_shape shape;
+  Dims dims;
+  WsLayout ws_lay;
+  int device;
+  void* kbuf[2];
+  void* vbuf[2];
+  int32_t* idx[2];
+  float* sel[2];
+  float* lse;
+  void* ws;
+  size_t device_bytes;
+  cudaEvent_t ev_idx[2], ev_ready[2], ev_free[2], ev_join;
+  // Timing: per layer PH_N events, plus the step's first and last.
+  std::vector<cudaEvent_t> tev;
+  cudaEvent_t t_begin, t_end;
+  int timed_layers;
+  int timed_launches;
+  bool timed_serial;
+};
+
+namespace {
+
+void ctx_free(dd_ctx* c) {
+  if (!c) return;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(c->device);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(c->kbuf[i]);
+    cudaFree(c->vbuf[i]);
+    cudaFree(c->idx[i]);
+    cudaFree(c->sel[i]);
+    if (c->ev_idx[i]) cudaEventDestroy(c->ev_idx[i]);
+    if (c->ev_ready[i]) cudaEventDestroy(c->ev_ready[i]);
+    if (c->ev_free[i]) cudaEventDestroy(c->ev_free[i]);
+  }
+  cudaFree(c->lse);
+  cudaFree(c->ws);
+  if (c->ev_join) cudaEventDestroy(c->ev_join);
+  for (cudaEvent_t e : c->tev) cudaEventDestroy(e);
+  if (c->t_begin) cudaEventDestroy(c->t_begin);
+  if (c->t_end) cudaEventDestroy(c->t_end);
+  if (prev >= 0) cudaSetDevice(prev);
+  delete c;
+}
+
+dd_status ensure_timing_events(dd_ctx* c, int n_layers) {
+  const size_t need = (size_t)n_layers * PH_N;
+  while (c->tev.size() < need) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return DD_ERR_CUDA;
+    c->tev.push_back(e);
+  }
+  if (!c->t_begin && cudaEventCreate(&c->t_begin) != cudaSuccess) return DD_ERR_CUDA;
+  if (!c->t_end && cudaEventCreate(&c->t_end) != cudaSuccess) return DD_ERR_CUDA;
+  return DD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+dd_status dd_ctx_create(const dd_shape* shape, dd_ctx** out) {
+  if (!out) return DD_ERR_INVALID_ARG;
+  *out = nullptr;
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  dd_ctx* c = new (std::nothrow) dd_ctx();
+  if (!c) return DD_ERR_OOM;
+  c->shape = *shape;
+  c->dims = d;
+  c->ws_lay = ws_layout(d);
+  if (cudaGetDevice(&c->device) != cudaSuccess) {
+    delete c;
+    return DD_ERR_CUDA;
+  }
+  const size_t rows_bytes = (size_t)d.U * d.k * d.d * d.elt;
+  const size_t idx_bytes = (size_t)d.U * d.k * sizeof(int32_t);
+  const size_t sel_bytes = (size_t)d.U * d.k * sizeof(float);
+  bool ok = true;
+  for (int i = 0; i < 2 && ok; ++i) {
+    ok = cudaMalloc(&c->kbuf[i], rows_bytes) == cudaSuccess &&
+         cudaMalloc(&c->vbuf[i], rows_bytes) == cudaSuccess &&
+         cudaMalloc((void**)&c->idx[i], idx_bytes) == cudaSuccess &&
+         cudaMalloc((void**)&c->sel[i], sel_bytes) == cudaSuccess;
+  }
+  ok = ok && cudaMalloc((void**)&c->lse, (size_t)d.B * d.Hq * sizeof(float)) == cudaSuccess;
+  ok = ok && cudaMalloc(&c->ws, c->ws_lay.total) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    ctx_free(c);
+    return DD_ERR_OOM;
+  }
+  c->device_bytes = 2 * (2 * rows_bytes + idx_bytes + sel_bytes) +
+                    (size_t)d.B * d.Hq * sizeof(float) + c->ws_lay.total;
+  for (int i = 0; i < 2 && ok; ++i)
+    ok = cudaEventCreateWithFlags(&c->ev_idx[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&c->ev_ready[i], cudaEventDisableTiming) == cudaSuccess &&
+         cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) == cudaSuccess;
+  if (!ok) {
+    ctx_free(c);
+    return DD_ERR_CUDA;
+  }
+  *out = c;
+  return DD_OK;
+}
+
+void dd_ctx_destroy(dd_ctx* ctx) { ctx_free(ctx); }
+
+size_t dd_ctx_device_bytes(const dd_ctx* ctx) { return ctx ? ctx->device_bytes : 0; }
+
+dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
+                         dd_stream_t compute, dd_stream_t copy, int flags) {
+  if (!c || !layers || n_layers < 1) return DD_ERR_INVALID_ARG;
+  const Dims& d = c->dims;
+  // Synchronous checks of every layer before anything is enqueued.
+  std::vector<const void*> kh(n_layers), vh(n_layers);
+  for (int l = 0; l < n_layers; ++l) {
+    const dd_layer_io& io = layers[l];
+    if (!io.q_spec || !io.q || !io.k_dev || !io.k_host || !io.v_host || !io.out)
+      return DD_ERR_INVALID_ARG;
+    if (d.W > 0 && !io.v_win) return DD_ERR_INVALID_ARG;
+    if (!aligned16(io.q_spec) || !aligned16(io.q) || !aligned16(io.k_dev) ||
+        !aligned16(io.k_host) || !aligned16(io.v_host) || !aligned16(io.out) ||
+        (io.v_win && !aligned16(io.v_win)))
+      return DD_ERR_INVALID_ARG;
+    kh[l] = host_to_device(io.k_host);
+    vh[l] = host_to_device(io.v_host);
+    if (!kh[l] || !vh[l]) return DD_ERR_INVALID_ARG;
+    if (!all_device({io.q_spec, io.q, io.k_dev, io.v_win, io.out})) return DD_ERR_INVALID_ARG;
+  }
+  const bool timing = (flags & DD_STEP_TIMING) != 0;
+  if (timing) {
+    dd_status st = ensure_timing_events(c, n_layers);
+    if (st != DD_OK) return st;
+  }
+  cudaStream_t C = reinterpret_cast<cudaStream_t>(compute);
+  cudaStream_t X = copy ? reinterpret_cast<cudaStream_t>(copy) : C;
+  const bool serial = (X == C);
+  char* ws = static_cast<char*>(c->ws);
+  float* logits = reinterpret_cast<float*>(ws + c->ws_lay.logits);
+  float2* part = reinterpret_cast<float2*>(ws + c->ws_lay.part);
+  float* attn_o = reinterpret_cast<float*>(ws + c->ws_lay.attn_o);
+  float2* attn_ml = reinterpret_cast<float2*>(ws + c->ws_lay.attn_ml);
+  auto T = [&](int l, int ph) { return c->tev[(size_t)l * PH_N + ph]; };
+  int launches = 0;
+#define DD_TRY(x)                                   \
+  do {                                              \
+    cudaError_t e_ = (x);                           \
+    if (e_ != cudaSuccess) return DD_ERR_CUDA;      \
+  } while (0)
+
+  // Steps 1-2 of layer l into index slot l % 2 (on the compute stream).
+  auto score_topk = [&](int l) -> cudaError_t {
+    const int s = l & 1;
+    if (timing) cudaEventRecord(T(l, PH_SCORE0), C);
+    cudaError_t e = launch_score(d, layers[l].q_spec, layers[l].k_dev, logits, part, C);
+    if (e != cudaSuccess) return e;
+    if (timing) cudaEventRecord(T(l, PH_SCORE1), C);
+    e = launch_topk(d, logits, part, c->idx[s], c->sel[s], c->lse, C);
+    if (e != cudaSuccess) return e;
+    if (timing) cudaEventRecord(T(l, PH_TOPK1), C);
+    launches += kScoreLaunches + kTopkLaunches;
+    return cudaEventRecord(c->ev_idx[s], C);
+  };
+  // Step 3 of layer l into scratch slot l % 2 (on the copy stream).
+  auto gather = [&](int l) -> cudaError_t {
+    const int s = l & 1;
+    cudaError_t e;
+    if (!serial) {
+      e = cudaStreamWaitEvent(X, c->ev_idx[s], 0);
+      if (e != cudaSuccess) return e;
+      e = cudaStreamWaitEvent(X, c->ev_free[s], 0);
+      if (e != cudaSuccess) return e;
+    }
+    if (timing) cudaEventRecord(T(l, PH_GATHER0), X);
+    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], X);
+    if (e != cudaSuccess) return e;
+    if (timing) cudaEventRecord(T(l, PH_GATHER1), X);
+    launches += kGatherLaunches;
+    return cudaEventRecord(c->ev_ready[s], X);
+  };
+  // Step 4 of layer l from scratch slot l % 2 (on the compute stream).
+  auto attend = [&](int l) -> cudaError_t {
+    const int s = l & 1;
+    cudaError_t e;
+    if (!serial) {
+      e = cudaStreamWaitEvent(C, c->ev_ready[s], 0);
+      if (e != cudaSuccess) return e;
+    }
+    if (timing) cudaEventRecord(T(l, PH_ATTN0), C);
+    e = launch_attn(d, layers[l].q, c->kbuf[s], c->vbuf[s], layers[l].k_dev, layers[l].v_win,
+                    layers[l].out, attn_o, attn_ml, C);
+    if (e != cudaSuccess) return e;
+    if (timing) cudaEventRecord(T(l, PH_ATTN1), C);
+    launches += kAttnLaunches;
+    return cudaEventRecord(c->ev_free[s], C);
+  };
+
+  if (timing) DD_TRY(cudaEventRecord(c->t_begin, C));
+  if (serial) {
+    for (int l = 0; l < n_layers; ++l) {
+      DD_TRY(score_topk(l));
+      DD_TRY(gather(l));
+      DD_TRY(attend(l));
+    }
+  } else {
+    // The copy stream starts after everything already queued on compute
+    // (the previous step may still be reading a scratch slot).
+    DD_TRY(cudaEventRecord(c->ev_join, C));
+    DD_TRY(cudaStreamWaitEvent(X, c->ev_join, 0));
+    DD_TRY(score_topk(0));
+    DD_TRY(gather(0));
+    for (int l = 0; l < n_layers; ++l) {
+      if (l + 1 < n_layers) {
+        DD_TRY(score_topk(l + 1));
+        DD_TRY(gather(l + 1));
+      }
+      DD_TRY(attend(l));
+    }
+    // Join: compute waits for the copy stream's last record.
+    DD_TRY(cudaEventRecord(c->ev_join, X));
+    DD_TRY(cudaStreamWaitEvent(C, c->ev_join, 0));
+  }
+  if (timing) {
+    DD_TRY(cudaEventRecord(c->t_end, C));
+    c->timed_layers = n_layers;
+    c->timed_launches = launches;
+    c->timed_serial = serial;
+  }
+#undef DD_TRY
+  return DD_OK;
+}
+
+dd_status dd_ctx_timings(dd_ctx* c, dd_phase_times* out) {
+  if (!c || !out) return DD_ERR_INVALID_ARG;
+  if (c->timed_layers <= 0) return DD_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(c->t_end) != cudaSuccess) return DD_ERR_CUDA;
+  memset(out, 0, sizeof(*out));
+  float ms = 0.f;
+  if (cudaEventElapsedTime(&ms, c->t_begin, c->t_end) != cudaSuccess) return DD_ERR_CUDA;
+  out->step_ms = ms;
+  for (int l = 0; l < c->timed_layers; ++l) {
+    const cudaEvent_t* e = &c->tev[(size_t)l * PH_N];
+    float a = 0.f;
+    if (cudaEventElapsedTime(&a, e[PH_SCORE0], e[PH_SCORE1]) != cudaSuccess) return DD_ERR_CUDA;
+    out->score_ms += a;
+    if (cudaEventElapsedTime(&a, e[PH_SCORE1], e[PH_TOPK1]) != cudaSuccess) return DD_ERR_CUDA;
+    out->topk_ms += a;
+    if (cudaEventElapsedTime(&a, e[PH_GATHER0], e[PH_GATHER1]) != cudaSuccess) return DD_ERR_CUDA;
+    out->gather_ms += a;
+    if (cudaEventElapsedTime(&a, e[PH_ATTN0], e[PH_ATTN1]) != cudaSuccess) return DD_ERR_CUDA;
+    out->attn_ms += a;
+  }
+  out->n_layers = c->timed_layers;
+  out->launches = c->timed_launches;
+  return DD_OK;
+}
+
+dd_status dd_ctx_score_times(dd_ctx* c, float* out_ms, int n) {
+  if (!c || !out_ms || n < 0) return DD_ERR_INVALID_ARG;
+  if (c->timed_layers <= 0) return DD_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(c->t_end) != cudaSuccess) return DD_ERR_CUDA;
+  for (int l = 0; l < c->timed_layers && l < n; ++l) {
+    const cudaEvent_t* e = &c->tev[(size_t)l * PH_N];
+    if (cudaEventElapsedTime(&out_ms[l], e[PH_SCORE0], e[PH_SCORE1]) != cudaSuccess)
+      return DD_ERR_CUDA;
+  }
+  return DD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,370 @@
+// Step 2 of the decode step: per (request, KV head) top-k of the selection
+// score, I = argtopk(a, k) over positions [0, n - W), ties to the lower
+// position, written in ascending position order.  (DualDecoder summary page,
+// core formulas: I = argtopk(alpha, k); paper Fig. 1 "Select Top-k".)
+//
+// The selection score is a[j] = exp(s_j - LSE) for MHA; since exp is
+// monotone the kernel ranks the fp32 logits themselves.  For grouped-query
+// heads a[j] = sum over the group of exp(s_hj - LSE_h) in fp32.  LSE_h is
+// first merged from the scoring kernel's per-chunk (max, sum) pairs.
+//
+// Exact radix select on order-preserving 32-bit keys, one CTA per unit:
+//   pass A  histogram of key bits 31..21 over the unit (global reads);
+//           the bucket b1 that holds the k-th largest key is found by a
+//           block scan from the top;
+//   pass B  every key with top bits >= b1 is compacted, in position order,
+//           into a shared-memory list (typically a few thousand entries);
+//   refine  bits 20..10 and 9..0 of the threshold key T are resolved on the
+//           list with two more histograms;
+//   emit    one ordered scan over the list writes every key > T plus the
+//           first (lowest-position) k_rem keys equal to T.
+// If the list would overflow shared memory (very many near-equal scores),
+// the refine and emit steps run over global memory instead: same result.
+#include <math.h>
+
+#include "dd_internal.cuh"
+
+namespace dd {
+namespace {
+
+constexpr int kTkThreads = 1024;
+constexpr int kTkWarps = kTkThreads / 32;
+constexpr int kPer = 4;                      // consecutive elements per thread
+constexpr int kTile = kTkThreads * kPer;     // elements per block-wide step
+constexpr int kListCap = 12288;
+
+struct TkSmem {
+  uint32_t hist[2048];
+  uint32_t wt[kTkWarps];
+  uint32_t res[2];
+  float lse[8];
+  uint32_t keys[kListCap];
+  int32_t idxs[kListCap];
+};
+
+// Order-preserving map float -> uint32 (larger float, larger key).
+__device__ __forceinline__ uint32_t f2key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key2f(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
+// Exclusive prefix sum of v over the block in thread order; *total = sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wt, uint32_t* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  if (lane == 31) wt[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t t = wt[lane];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(0xffffffffu, t, off);
+      if (lane >= off) t += y;
+    }
+    wt[lane] = t;
+  }
+  __syncthreads();
+  const uint32_t r = (warp ? wt[warp - 1] : 0u) + x - v;
+  *total = wt[kTkWarps - 1];
+  __syncthreads();
+  return r;
+}
+
+// Given a complete histogram, find the bin b with
+//   above(b) < k_rem <= above(b) + hist[b],  above(b) = sum_{x > b} hist[x],
+// and store (b, above(b)) in res.  Requires 1 <= k_rem <= sum(hist).
+__device__ void find_bin(const uint32_t* hist, int nbins, uint32_t k_rem, uint32_t* wt,
+                         uint32_t* res) {
+  const int per = nbins / kTkThreads;  // 1 or 2 bins per thread, top bins first
+  const int top = nbins - 1 - (int)threadIdx.x * per;
+  uint32_t local = 0;
+  for (int p = 0; p < per; ++p) local += hist[top - p];
+  uint32_t tot;
+  const uint32_t excl = block_excl_scan(local, wt, &tot);
+  if (excl < k_rem && k_rem <= excl + local) {
+    uint32_t acc = excl;
+    for (int p = 0; p < per; ++p) {
+      const uint32_t h = hist[top - p];
+      if (acc + h >= k_rem) {
+        res[0] = (uint32_t)(top - p);
+        res[1] = acc;
+        break;
+      }
+      acc += h;
+    }
+  }
+  __syncthreads();
+}
+
+// Keys of one unit read from the fp32 logits in global memory.
+template <int G>
+struct GlobalKeys {
+  const float* lg;  // logits row of the group's first query head
+  int ldn, span;
+  float lse[G];
+  // Keys of positions j0..j0+3 (j0 % 4 == 0, j0 < span); entries >= span
+  // hold unspecified values and must be masked by the caller.
+  __device__ __forceinline__ void load4(int j0, uint32_t (&key)[kPer], int32_t (&id)[kPer]) const {
+    if (G == 1) {
+      const float4 v = *reinterpret_cast<const float4*>(lg + j0);
+      key[0] = f2key(v.x);
+      key[1] = f2key(v.y);
+      key[2] = f2key(v.z);
+      key[3] = f2key(v.w);
+    } else {
+      float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float4 v = *reinterpret_cast<const float4*>(lg + (size_t)g * ldn + j0);
+        a[0] += __expf(v.x - lse[g]);
+        a[1] += __expf(v.y - lse[g]);
+        a[2] += __expf(v.z - lse[g]);
+        a[3] += __expf(v.w - lse[g]);
+      }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) key[e] = f2key(a[e]);
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) id[e] = j0 + e;
+  }
+  __device__ __forceinline__ int count() const { return span; }
+  __device__ __forceinline__ void get4(int e0, uint32_t (&key)[kPer], int32_t (&id)[kPer]) const {
+    if (e0 < span) load4(e0, key, id);
+  }
+};
+
+// Keys compacted into the shared-memory list.
+struct ListKeys {
+  const uint32_t* keys;
+  const int32_t* idxs;
+  int n;
+  __device__ __forceinline__ int count() const { return n; }
+  __device__ __forceinline__ void get4(int e0, uint32_t (&key)[kPer], int32_t (&id)[kPer]) const {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      if (e0 + e < n) {
+        key[e] = keys[e0 + e];
+        id[e] = idxs[e0 + e];
+      }
+    }
+  }
+};
+
+// Histogram of bits [lo, lo + nbits) of the keys whose bits above lo + nbits
+// equal `prefix` (all keys when nbits covers the top bits).
+template <class Src>
+__device__ void histogram(const Src& src, TkSmem& sm, int lo, int nbits, uint32_t prefix,
+                          bool filter) {
+  const int nb = 1 << nbits;
+  for (int i = threadIdx.x; i < nb; i += kTkThreads) sm.hist[i] = 0;
+  __syncthreads();
+  const int cnt = src.count();
+  for (int e0 = (int)threadIdx.x * kPer; e0 < cnt; e0 += kTile) {
+    uint32_t key[kPer];
+    int32_t id[kPer];
+    src.get4(e0, key, id);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      if (e0 + e < cnt) {
+        const bool take = !filter || (key[e] >> (lo + nbits)) == prefix;
+        if (take) atomicAdd(&sm.hist[(key[e] >> lo) & (uint32_t)(nb - 1)], 1u);
+      }
+    }
+  }
+  __syncthreads();
+}
+
+// Ordered emit: every key > T, then the first k_rem keys == T by position.
+template <class Src>
+__device__ void emit(const Src& src, TkSmem& sm, uint32_t T, uint32_t k_rem, int k,
+                     int32_t* idx_out, float* sel_out, bool mha, float lse0) {
+  const int cnt = src.count();
+  uint32_t cgt = 0, ceq = 0;
+  for (int t0 = 0; t0 < cnt; t0 += kTile) {
+    const int e0 = t0 + (int)threadIdx.x * kPer;
+    uint32_t key[kPer] = {0u, 0u, 0u, 0u};
+    int32_t id[kPer] = {0, 0, 0, 0};
+    src.get4(e0, key, id);
+    bool gt[kPer], eq[kPer];
+    uint32_t ngt = 0, neq = 0;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      const bool v = e0 + e < cnt;
+      gt[e] = v && key[e] > T;
+      eq[e] = v && key[e] == T;
+      ngt += gt[e];
+      neq += eq[e];
+    }
+    uint32_t tot;
+    const uint32_t ex = block_excl_scan(ngt | (neq << 16), sm.wt, &tot);
+    uint32_t gb = cgt + (ex & 0xFFFFu), eb = ceq + (ex >> 16);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) {
+      int pos = -1;
+      if (gt[e]) {
+        pos = (int)(gb + min(eb, k_rem));
+        ++gb;
+      } else if (eq[e]) {
+        if (eb < k_rem) pos = (int)(gb + eb);
+        ++eb;
+      }
+      if (pos >= 0 && pos < k) {
+        const float v = key2f(key[e]);
+        idx_out[pos] = id[e];
+        sel_out[pos] = mha ? expf(v - lse0) : v;
+      }
+    }
+    cgt += tot & 0xFFFFu;
+    ceq += tot >> 16;
+  }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kTkThreads, 1)
+    topk_kernel(const float* __restrict__ logits, const float2* __restrict__ part,
+                int32_t* __restrict__ idx_out, float* __restrict__ sel_out,
+                float* __restrict__ lse_out, int Hq, int Hkv, int ldn, int span, int k,
+                int nchunks) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  TkSmem& sm = *reinterpret_cast<TkSmem*>(smem_raw);
+  const int u = blockIdx.x, b = u / Hkv, hk = u - b * Hkv;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+
+  // LSE of each query head of the group from the per-chunk (max, sum) pairs.
+  if (warp < G) {
+    const float2* pp = part + (size_t)(u * G + warp) * nchunks;
+    float2 acc = make_float2(-INFINITY, 0.f);
+    for (int c = lane; c < nchunks; c += 32) acc = lse_merge(acc, pp[c]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      float2 o;
+      o.x = __shfl_xor_sync(0xffffffffu, acc.x, off);
+      o.y = __shfl_xor_sync(0xffffffffu, acc.y, off);
+      acc = lse_merge(acc, o);
+    }
+    if (lane == 0) {
+      const float lse = acc.x + logf(acc.y);
+      sm.lse[warp] = lse;
+      if (lse_out) lse_out[b * Hq + hk * G + warp] = lse;
+    }
+  }
+  __syncthreads();
+
+  GlobalKeys<G> src;
+  src.lg = logits + (size_t)(b * Hq + hk * G) * ldn;
+  src.ldn = ldn;
+  src.span = span;
+#pragma unroll
+  for (int g = 0; g < G; ++g) src.lse[g] = sm.lse[g];
+  int32_t* idx_u = idx_out + (size_t)u * k;
+  float* sel_u = sel_out + (size_t)u * k;
+
+  // Pass A: bucket of the k-th largest key by its top 11 bits.
+  histogram(src, sm, 21, 11, 0u, false);
+  find_bin(sm.hist, 2048, (uint32_t)k, sm.wt, sm.res);
+  const uint32_t b1 = sm.res[0];
+  const uint32_t above1 = sm.res[1];
+  const uint32_t in_b1 = sm.hist[b1];
+  uint32_t k_rem = (uint32_t)k - above1;
+  __syncthreads();
+
+  if (above1 + in_b1 <= (uint32_t)kListCap) {
+    // Pass B: ordered compaction of every key in buckets >= b1.
+    uint32_t nlist = 0;
+    for (int t0 = 0; t0 < span; t0 += kTile) {
+      const int j0 = t0 + (int)threadIdx.x * kPer;
+      uint32_t key[kPer] = {0u, 0u, 0u, 0u};
+      int32_t id[kPer];
+      if (j0 < span) src.load4(j0, key, id);
+      bool f[kPer];
+      uint32_t c = 0;
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        f[e] = (j0 + e < span) && (key[e] >> 21) >= b1;
+        c += f[e];
+      }
+      uint32_t tot;
+      uint32_t pos = nlist + block_excl_scan(c, sm.wt, &tot);
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) {
+        if (f[e]) {
+          sm.keys[pos] = key[e];
+          sm.idxs[pos] = j0 + e;
+          ++pos;
+        }
+      }
+      nlist += tot;
+    }
+    __syncthreads();
+    ListKeys list{sm.keys, sm.idxs, (int)nlist};
+    histogram(list, sm, 10, 11, b1, true);
+    find_bin(sm.hist, 2048, k_rem, sm.wt, sm.res);
+    const uint32_t b2 = sm.res[0];
+    k_rem -= sm.res[1];
+    __syncthreads();
+    const uint32_t pre = (b1 << 11) | b2;
+    histogram(list, sm, 0, 10, pre, true);
+    find_bin(sm.hist, 1024, k_rem, sm.wt, sm.res);
+    const uint32_t T = (pre << 10) | sm.res[0];
+    k_rem -= sm.res[1];
+    __syncthreads();
+    emit(list, sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
+  } else {
+    // Overflow: resolve the remaining bits and emit from global memory.
+    histogram(src, sm, 10, 11, b1, true);
+    find_bin(sm.hist, 2048, k_rem, sm.wt, sm.res);
+    const uint32_t b2 = sm.res[0];
+    k_rem -= sm.res[1];
+    __syncthreads();
+    const uint32_t pre = (b1 << 11) | b2;
+    histogram(src, sm, 0, 10, pre, true);
+    find_bin(sm.hist, 1024, k_rem, sm.wt, sm.res);
+    const uint32_t T = (pre << 10) | sm.res[0];
+    k_rem -= sm.res[1];
+    __syncthreads();
+    emit(src, sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
+  }
+}
+
+template <int G>
+cudaError_t launch_typed(const Dims& d, const float* logits, const float2* part, int32_t* idx,
+                         float* sel, float* lse, cudaStream_t st) {
+  // Opt in to more than 48 KB of dynamic shared memory, once per device.
+  static unsigned long long attr_done = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
+    e = cudaFuncSetAttribute(topk_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sizeof(TkSmem));
+    if (e != cudaSuccess) return e;
+    __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
+  }
+  topk_kernel<G><<<d.U, kTkThreads, sizeof(TkSmem), st>>>(logits, part, idx, sel, lse, d.Hq, d.Hkv,
+                                                          d.ldn, d.span, d.k, d.nchunks);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_topk(const Dims& d, const float* logits, const float2* part, int32_t* idx,
+                        float* sel, float* lse, cudaStream_t st) {
+  switch (d.G) {
+    case 1: return launch_typed<1>(d, logits, part, idx, sel, lse, st);
+    case 2: return launch_typed<2>(d, logits, part, idx, sel, lse, st);
+    case 4: return launch_typed<4>(d, logits, part, idx, sel, lse, st);
+    case 8: return launch_typed<8>(d, logits, part, idx, sel, lse, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dd

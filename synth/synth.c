@@ -77,6 +77,16 @@ double syn_normal(uint64_t base, uint64_t e) {
   return (e & 1) ? r * sin(th) : r * cos(th);
 }
 
+/* Both normals of pair p: elements 2p (cosine) and 2p+1 (sine). */
+static inline void syn_normal_pair(uint64_t base, uint64_t p, double* z0, double* z1) {
+  double u1 = syn_unif(base, 2 * p);
+  double u2 = syn_unif(base, 2 * p + 1);
+  double r = sqrt(-2.0 * log(u1));
+  double th = 6.283185307179586476925286766559 * u2;
+  *z0 = r * cos(th);
+  *z1 = r * sin(th);
+}
+
 static inline uint16_t f32_to_bf16_rne(float f) {
   uint32_t u;
   memcpy(&u, &f, 4);
@@ -149,9 +159,20 @@ typedef struct {
 
 static void fill_range(void* p, int64_t lo, int64_t hi) {
   fill_ctx* c = (fill_ctx*)p;
-  for (int64_t i = lo; i < hi; ++i)
-    store(c->out, c->dtype, i,
-          c->mean + c->sd * (float)syn_normal(c->base, c->offset + (uint64_t)i));
+  int64_t i = lo;
+  /* whole pairs of the stream where possible, single elements at the ends */
+  while (i < hi && ((c->offset + (uint64_t)i) & 1)) {
+    store(c->out, c->dtype, i, c->mean + c->sd * (float)syn_normal(c->base, c->offset + (uint64_t)i));
+    ++i;
+  }
+  for (; i + 1 < hi; i += 2) {
+    double z0, z1;
+    syn_normal_pair(c->base, (c->offset + (uint64_t)i) >> 1, &z0, &z1);
+    store(c->out, c->dtype, i, c->mean + c->sd * (float)z0);
+    store(c->out, c->dtype, i + 1, c->mean + c->sd * (float)z1);
+  }
+  if (i < hi)
+    store(c->out, c->dtype, i, c->mean + c->sd * (float)syn_normal(c->base, c->offset + (uint64_t)i));
 }
 
 void syn_fill_normal(uint64_t seed, uint64_t tag, uint64_t offset, int64_t count,
@@ -222,10 +243,20 @@ static void kv_range(void* p, int64_t lo, int64_t hi) {
       int64_t j = r % n, b = (r / n) / c->n_kv_heads;
       scale = (float)exp(0.5 * syn_normal(x->bscale, (uint64_t)(b * n + j)));
     }
-    for (int64_t t = 0; t < d; ++t) {
-      uint64_t e = (uint64_t)(r * d + t);
-      if (x->K) store(x->K, c->dtype, r * d + t, scale * (float)syn_normal(x->bk, e));
-      if (x->V) store(x->V, c->dtype, r * d + t, (float)syn_normal(x->bv, e));
+    /* d is even, so the row's elements are whole pairs of the stream */
+    for (int64_t t = 0; t < d; t += 2) {
+      uint64_t pr = (uint64_t)(r * d + t) >> 1;
+      double z0, z1;
+      if (x->K) {
+        syn_normal_pair(x->bk, pr, &z0, &z1);
+        store(x->K, c->dtype, r * d + t, scale * (float)z0);
+        store(x->K, c->dtype, r * d + t + 1, scale * (float)z1);
+      }
+      if (x->V) {
+        syn_normal_pair(x->bv, pr, &z0, &z1);
+        store(x->V, c->dtype, r * d + t, (float)z0);
+        store(x->V, c->dtype, r * d + t + 1, (float)z1);
+      }
     }
   }
 }

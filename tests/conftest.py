@@ -25,3 +25,10 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _built_library():
+    """Compile libdd.so (nvcc, sm_103a) if it is missing or stale."""
+    from sparse_kv_prefetch_gb300 import build
+    build.ensure_built()

@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/dd.h declares, and rejects bad arguments synchronously
+with the documented status codes, before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_kv_prefetch_gb300 as dd
+import synth
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        text = open(os.path.join(ROOT, "include", f)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(dd_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_function_is_exported():
+    lib = ctypes.CDLL(dd.LIB_PATH)
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings_and_version():
+    lib = dd.lib()
+    for s in range(6):
+        assert lib.dd_status_string(s)
+    assert lib.dd_status_string(99) == b"unknown status"
+    assert dd.version() >= 10000
+
+
+def _shape(**kw):
+    base = dict(batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, ctx_len=4096, top_k=64,
+                window=16, dtype=dd.DD_BF16)
+    base.update(kw)
+    return dd.Shape(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(window=4096), dd.DD_ERR_INVALID_ARG),          # W >= n
+    (dict(top_k=4096 - 15), dd.DD_ERR_INVALID_ARG),      # k > n - W
+    (dict(top_k=0), dd.DD_ERR_INVALID_ARG),
+    (dict(n_kv_heads=3), dd.DD_ERR_INVALID_ARG),         # H_q % H_kv != 0
+    (dict(batch=0), dd.DD_ERR_INVALID_ARG),
+    (dict(window=-1), dd.DD_ERR_INVALID_ARG),
+    (dict(head_dim=96), dd.DD_ERR_UNSUPPORTED),
+    (dict(head_dim=256, dtype=dd.DD_F32), dd.DD_ERR_UNSUPPORTED),
+    (dict(n_q_heads=6, n_kv_heads=2), dd.DD_ERR_UNSUPPORTED),  # group of 3
+    (dict(dtype=7), dd.DD_ERR_UNSUPPORTED),
+])
+def test_bad_shapes_rejected(kw, status):
+    n = ctypes.c_size_t()
+    st = dd.lib().dd_workspace_size(ctypes.byref(_shape(**kw).c()), ctypes.byref(n))
+    assert st == status
+
+
+def test_workspace_size_layout():
+    """Logits [B][H_q][round_up(n, 4)] fp32 dominate; the rest is small."""
+    for w in (synth.C1, synth.C2, synth.C3, synth.C4, synth.C5):
+        shp = dd.Shape(w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.ctx_len, w.top_k,
+                       w.window, w.dtype)
+        ws = dd.workspace_size(shp)
+        logits = w.batch * w.n_q_heads * ((w.ctx_len + 3) // 4 * 4) * 4
+        assert logits <= ws <= logits * 1.1 + (1 << 20)
+        assert ws % 256 == 0
+
+
+def test_null_and_misaligned_pointers_rejected():
+    lib = dd.lib()
+    shp = _shape().c()
+    st = lib.dd_score_topk(ctypes.byref(shp), None, 16, 16, 16, None, 16, 1 << 30, None)
+    assert st == dd.DD_ERR_INVALID_ARG
+    st = lib.dd_score_topk(ctypes.byref(shp), 17, 16, 16, 16, None, 16, 1 << 30, None)
+    assert st == dd.DD_ERR_INVALID_ARG
+    st = lib.dd_sparse_decode_attn(ctypes.byref(shp), 16, 16, 16, 16, None, 16, 16, 1 << 30,
+                                   None)  # W > 0 needs the window V
+    assert st == dd.DD_ERR_INVALID_ARG
+    st = lib.dd_gather_h2d(ctypes.byref(shp), 16, 16, 16, 16, 16, 1, None)
+    assert st == dd.DD_ERR_UNSUPPORTED  # only the zero-copy mode exists
+    st = lib.dd_score_topk(ctypes.byref(shp), 16, 16, 16, 16, None, 16, 1024, None)
+    assert st == dd.DD_ERR_INVALID_ARG  # workspace too small
+    assert lib.dd_decode_step(None, None, 0, None, None, 0) == dd.DD_ERR_INVALID_ARG
+
+
+def test_pageable_host_store_rejected_by_binding():
+    import torch
+    shp = _shape()
+    t = torch.empty(16, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        dd.gather_h2d(shp, t, t, 16, 16, 16)
+
+
+def test_product_path_never_touches_the_oracle():
+    """The package and its sources import neither the oracle nor the generator."""
+    pkg = os.path.join(ROOT, "sparse_kv_prefetch_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"\b(import|from)\s+(oracle|synth)\b", text), f
+                assert "liboracle" not in text and "libsynth" not in text, f

@@ -1,0 +1,197 @@
+"""GPU path against the fp64 oracle, through the C ABI (libdd.so).
+
+Small cases cover every unit of several tiles with ragged tails, every
+supported head size, MHA and grouped-query heads, and the degenerate cases
+(k = n - W, k = 1 with no window, exact ties).  The full-size cases run each
+workload's per-layer shape in the launch configuration the benchmark times and
+check sampled units.
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_kv_prefetch_gb300 as dd
+import synth
+from gpu_util import (Outputs, Slot, check_gather, check_unit_attention, check_unit_topk,
+                      dd_shape, orc_shape, run_layer, sample_units, TOL_OUT)
+
+pytestmark = pytest.mark.gpu
+
+C1, C2, C3, C4, C5 = synth.C1, synth.C2, synth.C3, synth.C4, synth.C5
+
+SMALL = {
+    "c1": C1,
+    "c2_mini": C2.scaled(batch=2, n_q_heads=4, n_kv_heads=4, ctx_len=5000),
+    "ragged_n": C2.scaled(batch=1, n_q_heads=2, n_kv_heads=2, ctx_len=3001, top_k=50, window=7,
+                          n_planted=9),
+    "c3_mini": C3.scaled(batch=1, n_q_heads=2, n_kv_heads=2, ctx_len=20000),
+    "c4_mini": C4.scaled(batch=2, n_q_heads=3, n_kv_heads=3, ctx_len=9000),
+    "c5_mini": C5.scaled(batch=2, n_q_heads=8, n_kv_heads=2, ctx_len=12000),
+    "gqa2_d64": C2.scaled(batch=2, n_q_heads=4, n_kv_heads=2, head_dim=64, ctx_len=4096,
+                          top_k=100, window=16, n_planted=20),
+    "gqa8_d256": C2.scaled(batch=1, n_q_heads=16, n_kv_heads=2, head_dim=256, ctx_len=2500,
+                           top_k=64, window=32, n_planted=8),
+    "f32_d128": C1.scaled(batch=2, n_q_heads=2, n_kv_heads=2, head_dim=128, ctx_len=3000,
+                          top_k=200, window=8, n_planted=10),
+    "f32_gqa2_d64": C1.scaled(batch=1, n_q_heads=4, n_kv_heads=2, ctx_len=2600, top_k=80,
+                              window=0, n_planted=12),
+}
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_layer_small(name):
+    w = SMALL[name]
+    s = Slot(w)
+    o = Outputs(w)
+    run_layer(w, s, o)
+    torch.cuda.synchronize()
+    idx, sel, lse = o.idx.cpu().numpy(), o.sel.cpu().numpy(), o.lse.cpu().numpy()
+    out = o.out.cpu().numpy()
+    for u in range(w.units):
+        check_unit_topk(w, s, u, idx[u], sel[u], lse)
+        check_unit_attention(w, s, u, idx[u], out)
+        if w.n_planted:
+            b, hk = divmod(u, w.n_kv_heads)
+            assert set(s.planted[b, hk, :w.n_planted].tolist()) <= set(idx[u].tolist())
+    check_gather(w, s, idx, o.k_buf, o.v_buf, range(w.units))
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_k_equals_span_is_dense_attention(dtype):
+    """k = n - W selects every candidate: the result is dense softmax attention."""
+    w = C2.scaled(batch=1, n_q_heads=4, n_kv_heads=2, head_dim=64, ctx_len=700, top_k=700 - 20,
+                  window=20, dtype=dtype, n_planted=4)
+    s = Slot(w)
+    o = Outputs(w)
+    run_layer(w, s, o)
+    torch.cuda.synchronize()
+    idx, out = o.idx.cpu().numpy(), o.out.cpu().numpy()
+    orc = oracle.get()
+    for u in range(w.units):
+        assert idx[u].tolist() == list(range(700 - 20))
+        b, hk = divmod(u, w.n_kv_heads)
+        dense = orc.dense_unit(orc_shape(w), s.q_h, s.K_h, s.V_h, b, hk)
+        got = out[b, hk * w.group:(hk + 1) * w.group]
+        assert np.max(np.abs(got - dense)) <= TOL_OUT[dtype]
+
+
+def test_top1_without_window_returns_that_value_row():
+    """k = 1, W = 0: the softmax over one row is 1, so o = V[argmax a]."""
+    w = C2.scaled(batch=2, n_q_heads=2, n_kv_heads=2, ctx_len=1000, top_k=1, window=0,
+                  n_planted=1)
+    s = Slot(w)
+    o = Outputs(w)
+    run_layer(w, s, o)
+    torch.cuda.synchronize()
+    idx, out = o.idx.cpu().numpy(), o.out.cpu()
+    for u in range(w.units):
+        b, hk = divmod(u, w.n_kv_heads)
+        assert idx[u, 0] == s.planted[b, hk, 0]
+        assert torch.equal(out[b, hk], s.V_h[b, hk, idx[u, 0]].float())
+
+
+@pytest.mark.parametrize("n", [3000, 20000])
+def test_exact_ties_take_lowest_positions(n):
+    """q_spec = 0 makes every logit 0: the selection is positions 0..k-1.
+    n = 20000 overflows the shared-memory candidate list (global path)."""
+    w = C2.scaled(batch=1, n_q_heads=2, n_kv_heads=2, ctx_len=n, top_k=300, window=10,
+                  n_planted=0, plant_mode=synth.PLANT_NONE)
+    s = Slot(w)
+    s.q_spec_h.zero_()
+    s.to_device()
+    o = Outputs(w)
+    run_layer(w, s, o)
+    torch.cuda.synchronize()
+    idx, sel, lse = o.idx.cpu().numpy(), o.sel.cpu().numpy(), o.lse.cpu().numpy()
+    for u in range(w.units):
+        assert idx[u].tolist() == list(range(300))
+        np.testing.assert_allclose(lse[0, u], np.log(n), atol=1e-3)
+        np.testing.assert_allclose(sel[u], 1.0 / n, rtol=2e-3)
+        check_unit_attention(w, s, u, idx[u], o.out.cpu().numpy())
+
+
+def _layers(w, slots, outs, L):
+    return [dd.LayerIO(slots[l % len(slots)].q_spec, slots[l % len(slots)].q,
+                       slots[l % len(slots)].K, slots[l % len(slots)].K_h,
+                       slots[l % len(slots)].V_h, slots[l % len(slots)].v_win, outs[l])
+            for l in range(L)]
+
+
+@pytest.mark.parametrize("name", ["c1", "c2_mini", "c5_mini"])
+def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
+    """The two-stream layer loop gives bit-identical outputs to the serial
+    schedule and to the standalone per-layer calls (cycled slots)."""
+    w = SMALL[name]
+    D, L = 2, 5
+    slots = [Slot(w, d) for d in range(D)]
+    ref = []
+    for d in range(D):
+        o = Outputs(w)
+        run_layer(w, slots[d], o)
+        ref.append(o.out)
+    ctx = dd.Ctx(dd_shape(w))
+    outs_a = [torch.full((w.batch, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
+              for _ in range(L)]
+    outs_b = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
+    compute = torch.cuda.Stream()
+    copy = torch.cuda.Stream(priority=-1)
+    compute.wait_stream(torch.cuda.current_stream())
+    ctx.decode_step(_layers(w, slots, outs_a, L), compute=compute, copy=copy, timing=True)
+    t = ctx.timings()
+    ctx.decode_step(_layers(w, slots, outs_b, L), compute=compute, copy=None)
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert torch.equal(outs_a[l], outs_b[l]), f"layer {l}: overlapped != serial"
+        assert torch.equal(outs_a[l], ref[l % D]), f"layer {l}: step != per-layer calls"
+    assert t["n_layers"] == L and t["launches"] == L * 5
+    assert t["step_ms"] > 0 and t["score_ms"] > 0 and t["gather_ms"] > 0
+    ctx.close()
+
+
+FULL = {"c2": C2, "c3": C3, "c4": C4, "c5": C5}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_size_layer_sampled_units(name):
+    """One layer at the workload's full per-layer size, through the layer loop
+    (the benchmark's launch configuration); sampled units against the oracle."""
+    w = FULL[name]
+    s = Slot(w)
+    o = Outputs(w)
+    run_layer(w, s, o)
+    ctx = dd.Ctx(dd_shape(w))
+    outs = [torch.empty_like(o.out) for _ in range(2)]
+    compute = torch.cuda.Stream()
+    copy = torch.cuda.Stream(priority=-1)
+    compute.wait_stream(torch.cuda.current_stream())
+    ctx.decode_step(_layers(w, [s], outs, 2), compute=compute, copy=copy)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], o.out) and torch.equal(outs[1], o.out)
+    idx, sel, lse = o.idx.cpu().numpy(), o.sel.cpu().numpy(), o.lse.cpu().numpy()
+    out = o.out.cpu().numpy()
+    units = sample_units(w.units, n=5, seed=w.cfg_id)
+    for u in units:
+        check_unit_topk(w, s, u, idx[u], sel[u], lse)
+        check_unit_attention(w, s, u, idx[u], out)
+        if w.n_planted:
+            b, hk = divmod(u, w.n_kv_heads)
+            assert set(s.planted[b, hk, :w.n_planted].tolist()) <= set(idx[u].tolist())
+    check_gather(w, s, idx, o.k_buf, o.v_buf, units)
+    # properties that hold for every unit: ascending, in range, planted keys kept
+    assert np.all(np.diff(idx, axis=1) > 0) and idx.min() >= 0 and idx.max() < w.ctx_len - w.window
+    if w.n_planted:
+        P = w.n_planted
+        for u in range(w.units):
+            b, hk = divmod(u, w.n_kv_heads)
+            assert np.all(np.isin(s.planted[b, hk, :P], idx[u]))
+    ctx.close()
+    del s, o, outs
+    _free()
