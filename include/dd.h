@@ -150,6 +150,36 @@ dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void
                                 float* out, void* workspace, size_t ws_bytes,
                                 dd_stream_t stream);
 
+/*
+ * The paper has no counterpart to this call.  It is dd_sparse_decode_attn
+ * without the workspace argument, for callers that cannot allocate device
+ * memory at all.  Examples: an engine that has already promised every free
+ * byte of HBM to its KV-cache pool, or a plugin inside a framework that owns
+ * all device allocations.  It also helps loops that must not stall the GPU:
+ * cudaMalloc synchronises the device.  The call itself calls no allocator.
+ *
+ * The split-k partials live in one static device array of
+ * DD_NOALLOC_SCRATCH_BYTES inside libdd.so.  Every GPU that loads the
+ * library holds that array until the process exits.  A shape needs
+ * round_up(B*H_q*S*d*4, 256) + B*H_q*S*8 bytes of it, where
+ * S = ceil((k + W) / 64).  Larger shapes return DD_ERR_UNSUPPORTED and
+ * enqueue nothing.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current.  That first call should
+ * come before any stream capture.
+ *
+ * All calls share the array, and it keeps the last call's contents.  Nothing
+ * in it needs to start at zero.  Calls that overlap on the GPU race on it, so
+ * the caller must serialise them (one stream, or explicit ordering).
+ * Arguments, layouts, results and errors are otherwise those of
+ * dd_sparse_decode_attn.
+ */
+#define DD_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
+dd_status dd_sparse_decode_attn_noalloc(const dd_shape* shape, const void* q, const void* k_buf,
+                                        const void* v_buf, const void* k_dev, const void* v_win,
+                                        float* out, dd_stream_t stream);
+
 /* ---------------------------- layer loop ---------------------------- */
 
 typedef struct dd_ctx dd_ctx;

@@ -84,6 +84,7 @@ def _lib():
             "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dd_gather_h2d": ([S, P, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
             "dd_sparse_decode_attn": ([S, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
+            "dd_sparse_decode_attn_noalloc": ([S, P, P, P, P, P, P, P], ctypes.c_int),
             "dd_ctx_create": ([S, ctypes.POINTER(P)], ctypes.c_int),
             "dd_ctx_destroy": ([P], None),
             "dd_ctx_device_bytes": ([P], ctypes.c_size_t),
@@ -178,6 +179,19 @@ def sparse_decode_attn(shape: Shape, q, k_buf, v_buf, k_dev, v_win, out, workspa
                                         _dev(v_buf), _dev(k_dev), _dev(v_win), _dev(out),
                                         _dev(workspace), ws_bytes, _stream(stream)),
            "dd_sparse_decode_attn")
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def sparse_decode_attn_noalloc(shape: Shape, q, k_buf, v_buf, k_dev, v_win, out, stream=None):
+    """Step 4 without a workspace: the partials use the library's static device
+    array (NOALLOC_SCRATCH_BYTES, shared by every call; calls must not overlap
+    on the GPU).  For callers that cannot allocate device memory; see dd.h."""
+    _check(_lib().dd_sparse_decode_attn_noalloc(ctypes.byref(shape.c()), _dev(q), _dev(k_buf),
+                                                _dev(v_buf), _dev(k_dev), _dev(v_win),
+                                                _dev(out), _stream(stream)),
+           "dd_sparse_decode_attn_noalloc")
 
 
 class LayerIO(NamedTuple):
