@@ -46,6 +46,8 @@ def parse():
     p.add_argument("--workload", default=synth.C2.name, choices=list(synth.WORKLOADS))
     p.add_argument("--profile-case", action="store_true",
                    help="small case for ncu captures: batch 2, 2 layers, 1 slot")
+    p.add_argument("--late-gather", type=int, default=0,
+                   help="1: start each layer's gather after the previous attention")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU work budget of the oracle baseline")
     return p.parse_args()
@@ -262,8 +264,35 @@ def run_ours(args, rank, world):
     probe_gbs = statistics.median(probe)
     del dst
 
+    # The gather alone (no other kernel running), cycling over every layer
+    # slot so that each call meets cold host pages, as inside a decode step.
+    U = B * Hkv
+    g_idx = torch.empty((D, U, k), dtype=torch.int32, device=dev)
+    g_sel = torch.empty((U, k), dtype=torch.float32, device=dev)
+    g_lse = torch.empty((B, Hq), dtype=torch.float32, device=dev)
+    g_ws = torch.empty(dd.workspace_size(shape), dtype=torch.uint8, device=dev)
+    g_kb = torch.empty((U, k, d), dtype=dt, device=dev)
+    g_vb = torch.empty_like(g_kb)
+    for s_ in range(D):
+        dd.score_topk(shape, qs_d[s_], K_d[s_], g_idx[s_], g_sel, g_lse, g_ws, stream=compute)
+    gather_alone = {}
+    for mode in (0, 1):
+        for i in range(2 * D):
+            dd.gather_h2d(shape, K_h[i % D], V_h[i % D], g_idx[i % D], g_kb, g_vb, mode=mode,
+                          stream=compute)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(compute)
+        for i in range(4 * D):
+            dd.gather_h2d(shape, K_h[i % D], V_h[i % D], g_idx[i % D], g_kb, g_vb, mode=mode,
+                          stream=compute)
+        e1.record(compute)
+        e1.synchronize()
+        gather_alone[mode] = w.gather_bytes() * 4 * D / (e0.elapsed_time(e1) * 1e-3) / 1e9
+    del g_ws, g_kb, g_vb
+
     def step(copy_stream, timing=True):
-        ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing)
+        ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
+                        late_gather=args.late_gather)
         return ctx.timings() if timing else None
 
     compute.wait_stream(torch.cuda.current_stream())
@@ -312,7 +341,7 @@ def run_ours(args, rank, world):
         with torch.cuda.stream(compute):
             qs_l.copy_(qs_src, non_blocking=True)
             q_l.copy_(q_src, non_blocking=True)
-        ctx.decode_step(layers_e2e, compute=compute, copy=copy)
+        ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=args.late_gather)
         with torch.cuda.stream(compute):
             out_h.copy_(outs, non_blocking=True)
     for _ in range(2):
@@ -365,14 +394,19 @@ def run_ours(args, rank, world):
                 "q = q_spec + N(0, 0.1^2)",
         "config": config_of(w, args),
         "scoring_hbm_gbs": score_gbs,
-        "gather_host_link_gbs": gather_gbs,
+        "gather_host_link_gbs": gather_alone[0],
+        "gather_frac_of_probe": gather_alone[0] / probe_gbs,
         "host_link_probe_gbs": probe_gbs,
-        "gather_frac_of_probe": gather_gbs / probe_gbs,
+        "gather_alone_gbs": {"bulk_copy": gather_alone[0], "load_store": gather_alone[1]},
+        "gather_in_step_gbs": gather_gbs,
         "hidden_fraction": hidden,
         "hidden_bound": min(1.0, comp_ser / g_ser) if g_ser > 0 else None,
         "phase_ms_per_step": {kk: statistics.mean(p[kk] for p in phases)
                               for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms", "attn_ms")},
         "serial_step_ms": t_ser,
+        "serial_phase_ms_per_step": {kk: statistics.mean(p[kk] for p in serial)
+                                     for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms",
+                                                "attn_ms")},
         "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": score_gbs / peak, "traffic": None,

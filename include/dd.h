@@ -67,7 +67,7 @@ typedef enum {
   DD_ERR_UNSUPPORTED = 2, /* shape or dtype outside the supported set */
   DD_ERR_OOM = 3,         /* device allocation failed (dd_ctx_create only) */
   DD_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed */
-  DD_ERR_TIMEOUT = 5      /* reserved: a bounded device-side wait gave up */
+  DD_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (dd_check_device) */
 } dd_status;
 
 typedef enum { DD_F32 = 0, DD_BF16 = 1 } dd_dtype;
@@ -92,6 +92,16 @@ const char* dd_status_string(int status);
 
 /* Library version, major * 10000 + minor * 100 + patch. */
 int dd_version(void);
+
+/*
+ * Every wait inside the library's kernels (on an mbarrier that a bulk copy
+ * completes) is bounded: after 2 s the kernel records the timeout in a
+ * device-side status word, lets its copies in flight land and returns, so the
+ * context stays usable.  This call synchronises the current device, returns
+ * DD_ERR_TIMEOUT if any wait gave up since the previous call (DD_ERR_CUDA if
+ * the device reports an error) and clears the status words.
+ */
+dd_status dd_check_device(void);
 
 /*
  * Bytes of device workspace that dd_score_topk and dd_sparse_decode_attn need
@@ -121,15 +131,19 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
 /*
  * Step 3 for one layer: for every unit u and slot i < k, copy row
  * idx[u][i] of the pinned host K and V stores into row i of k_buf / v_buf.
- * The rows are read by the GPU directly from page-locked host memory
- * (zero-copy loads through unified addressing, over the host link).
+ * The rows are read by the GPU directly from page-locked host memory through
+ * unified addressing, over the host link (zero-copy).
  *   k_host, v_host  pinned host [B][H_kv][n][d]
  *   idx             device [B][H_kv][k] int32, each in [0, n); an index
  *                   outside that range is clamped into it on the device, so
  *                   the kernel never reads outside the store
  *   k_buf, v_buf    device [B][H_kv][k][d]
- *   mode            0 = zero-copy gather kernel (the only mode; others
- *                   return DD_ERR_UNSUPPORTED)
+ *   mode            0 = bulk-copy gather: one-warp CTAs issue one
+ *                       cp.async.bulk per row into shared memory and write
+ *                       tiles back with bulk stores (used by dd_decode_step);
+ *                   1 = load/store gather: 16-byte loads from every thread;
+ *                   other values return DD_ERR_UNSUPPORTED.  Both modes give
+ *                   identical bytes.
  */
 dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v_host,
                         const int32_t* idx, void* k_buf, void* v_buf, int mode,
@@ -208,7 +222,9 @@ void dd_ctx_destroy(dd_ctx* ctx);
 size_t dd_ctx_device_bytes(const dd_ctx* ctx);
 
 enum {
-  DD_STEP_TIMING = 1 /* record per-phase CUDA events; read with dd_ctx_timings */
+  DD_STEP_TIMING = 1,     /* record per-phase CUDA events; read with dd_ctx_timings */
+  DD_STEP_LATE_GATHER = 2 /* start the gather of layer l+1 after the attention of
+                             layer l (it then overlaps the scoring of layer l+2) */
 };
 
 /*

@@ -23,6 +23,7 @@ LIB_PATH = os.path.join(_HERE, "libdd.so")
 DD_OK, DD_ERR_INVALID_ARG, DD_ERR_UNSUPPORTED, DD_ERR_OOM, DD_ERR_CUDA, DD_ERR_TIMEOUT = range(6)
 DD_F32, DD_BF16 = 0, 1
 DD_STEP_TIMING = 1
+DD_STEP_LATE_GATHER = 2
 
 
 class DDError(RuntimeError):
@@ -80,6 +81,7 @@ def _lib():
         sig = {
             "dd_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "dd_version": ([], ctypes.c_int),
+            "dd_check_device": ([], ctypes.c_int),
             "dd_workspace_size": ([S, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
             "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dd_gather_h2d": ([S, P, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
@@ -145,6 +147,11 @@ def _stream(s) -> Optional[int]:
 
 def version() -> int:
     return _lib().dd_version()
+
+
+def check_device():
+    """Raise DDError(DD_ERR_TIMEOUT) if a bounded device-side wait gave up."""
+    _check(_lib().dd_check_device(), "dd_check_device")
 
 
 def workspace_size(shape: Shape) -> int:
@@ -238,13 +245,14 @@ class Ctx:
                                  _host(io.v_host), _dev(io.v_win), _dev(io.out))
         return arr
 
-    def decode_step(self, layers, compute=None, copy=None, timing: bool = False):
+    def decode_step(self, layers, compute=None, copy=None, timing: bool = False,
+                    late_gather: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
-        _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs,
-                                     DD_STEP_TIMING if timing else 0), "dd_decode_step")
+        flags = (DD_STEP_TIMING if timing else 0) | (DD_STEP_LATE_GATHER if late_gather else 0)
+        _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 
     def timings(self) -> dict:

@@ -143,6 +143,13 @@ const char* dd_status_string(int s) {
 
 int dd_version(void) { return DD_VERSION; }
 
+dd_status dd_check_device(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return DD_ERR_CUDA;
+  const unsigned int a = take_score_status();
+  const unsigned int b = take_gather_status();
+  return (a | b) ? DD_ERR_TIMEOUT : DD_OK;
+}
+
 dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes) {
   if (!bytes) return DD_ERR_INVALID_ARG;
   Dims d;
@@ -179,7 +186,7 @@ dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v
   Dims d;
   dd_status st = resolve(shape, &d);
   if (st != DD_OK) return st;
-  if (mode != 0) return DD_ERR_UNSUPPORTED;
+  if (mode != 0 && mode != 1) return DD_ERR_UNSUPPORTED;
   if (!k_host || !v_host || !idx || !k_buf || !v_buf) return DD_ERR_INVALID_ARG;
   if (!aligned16(k_host) || !aligned16(v_host) || !aligned16(k_buf) || !aligned16(v_buf))
     return DD_ERR_INVALID_ARG;
@@ -187,8 +194,8 @@ dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v
   const void* vh = host_to_device(v_host);
   if (!kh || !vh) return DD_ERR_INVALID_ARG;
   if (!all_device({idx, k_buf, v_buf})) return DD_ERR_INVALID_ARG;
-  return cuda_status(
-      launch_gather(d, kh, vh, idx, k_buf, v_buf, reinterpret_cast<cudaStream_t>(stream)));
+  return cuda_status(launch_gather(d, kh, vh, idx, k_buf, v_buf, mode,
+                                   reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void* k_buf,
@@ -398,7 +405,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       if (e != cudaSuccess) return e;
     }
     if (timing) cudaEventRecord(T(l, PH_GATHER0), X);
-    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], X);
+    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], 0, X);
     if (e != cudaSuccess) return e;
     if (timing) cudaEventRecord(T(l, PH_GATHER1), X);
     launches += kGatherLaunches;
@@ -435,12 +442,17 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     DD_TRY(cudaStreamWaitEvent(X, c->ev_join, 0));
     DD_TRY(score_topk(0));
     DD_TRY(gather(0));
+    const bool late = (flags & DD_STEP_LATE_GATHER) != 0;
     for (int l = 0; l < n_layers; ++l) {
-      if (l + 1 < n_layers) {
-        DD_TRY(score_topk(l + 1));
+      if (l + 1 < n_layers) DD_TRY(score_topk(l + 1));
+      if (l + 1 < n_layers && !late) DD_TRY(gather(l + 1));
+      DD_TRY(attend(l));
+      if (l + 1 < n_layers && late) {
+        // Late gather: layer l+1's rows move only after layer l's attention,
+        // so the gather overlaps the scoring of layer l+2, not the attention.
+        DD_TRY(cudaStreamWaitEvent(X, c->ev_free[l & 1], 0));
         DD_TRY(gather(l + 1));
       }
-      DD_TRY(attend(l));
     }
     // Join: compute waits for the copy stream's last record.
     DD_TRY(cudaEventRecord(c->ev_join, X));

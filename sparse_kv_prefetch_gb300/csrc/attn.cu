@@ -182,6 +182,10 @@ template <typename T, int D, int G>
 cudaError_t launch_typed(const Dims& d, const void* q, const void* kb, const void* vb,
                          const void* kd, const void* vw, float* out, float* po, float2* pml,
                          cudaStream_t st) {
+  static unsigned long long prepared = 0, prepared_merge = 0;
+  cudaError_t e0 = prepare_kernel(attn_partial_kernel<T, D, G>, &prepared, 0);
+  if (e0 == cudaSuccess) e0 = prepare_kernel(attn_merge_kernel, &prepared_merge, 0);
+  if (e0 != cudaSuccess) return e0;
   const float scale = 1.0f / sqrtf((float)d.d);
   const dim3 grid((unsigned)d.U, (unsigned)d.nsplit);
   attn_partial_kernel<T, D, G><<<grid, kAttnThreads, 0, st>>>(

@@ -38,7 +38,8 @@ cudaError_t launch_score(const Dims& d, const void* q_spec, const void* k_dev, f
 cudaError_t launch_topk(const Dims& d, const float* logits, const float2* part, int32_t* idx,
                         float* sel, float* lse, cudaStream_t st);
 cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
-                          const int32_t* idx, void* k_buf, void* v_buf, cudaStream_t st);
+                          const int32_t* idx, void* k_buf, void* v_buf, int mode,
+                          cudaStream_t st);
 cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const void* v_buf,
                         const void* k_dev, const void* v_win, float* out, float* part_o,
                         float2* part_ml, cudaStream_t st);
@@ -48,8 +49,36 @@ constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 1, kAttnL
 
 int sm_count();
 
+// Once per device and kernel: opt in to `dyn_smem` bytes of dynamic shared
+// memory (if above the default 48 KB) and ask for the largest shared-memory
+// carveout.  Every kernel of the library asks for the same carveout, so the
+// SMs never need a different L1/shared split to host kernels of the compute
+// and copy streams side by side.
+template <typename Kernel>
+cudaError_t prepare_kernel(Kernel* fn, unsigned long long* done_mask, int dyn_smem) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  if (dyn_smem > 48 * 1024) {
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, dyn_smem);
+    if (e != cudaSuccess) return e;
+  }
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
+  return cudaSuccess;
+}
+
 // Keys per scoring CTA for a stored dtype and head size (0 if unsupported).
 int score_chunk(int dtype, int head_dim);
+
+// Read and clear the device-side status words that kernels set when a bounded
+// wait gives up (nonzero: some wait timed out since the last read).
+unsigned int take_score_status();
+unsigned int take_gather_status();
 
 // ----------------------------------------------------------------- device
 
@@ -93,6 +122,80 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
 __device__ __forceinline__ uint4 ld_ro(const void* p) {
   return __ldg(reinterpret_cast<const uint4*>(p));
 }
+
+// ------------------------------------------------ async copies (TMA, mbarrier)
+//
+// Bulk copies (cp.async.bulk) move contiguous byte ranges between global and
+// shared memory on the SM's tensor-memory-access unit, without occupying the
+// load/store pipeline; completion is signalled on an mbarrier in shared memory
+// through its transaction count.
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+// Make the initialised barriers visible to the async (bulk-copy) proxy.
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Every wait in this library is bounded: after kWaitLimitNs the wait gives up
+// and returns false; the caller records DD_ERR_TIMEOUT and stops its work.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+// global -> shared, completion counted on `bar` (bytes and addresses 16-aligned).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+// shared -> global, tracked by the issuing thread's bulk async-groups.
+__device__ __forceinline__ void bulk_store(void* gmem_dst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// Wait until the committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Wait until the committed bulk stores are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Merge two (max, sum of exp(x - max)) pairs.
 __device__ __forceinline__ float2 lse_merge(float2 a, float2 b) {

@@ -4,32 +4,141 @@
 // over the context, so they are gathered from host memory across the
 // host-to-device link; summary page worked example, step 5.)
 //
-// The SMs read host memory directly (zero-copy: page-locked memory is mapped
-// into the GPU's unified address space), so the scattered rows never need a
-// host-side gather or one copy-engine request per row.  Consecutive threads
-// read consecutive 16-byte pieces of a row (a row of d elements is d*elt/16
-// pieces; K and V pieces of the same row are adjacent), and every thread keeps
-// kInFlight independent host loads outstanding to cover the link latency.
-// The grid is small on purpose: it must leave room for the scoring kernel
-// that runs concurrently on the compute stream.
+// The GPU reads host memory directly (zero-copy: page-locked memory is
+// mapped into its unified address space), so the scattered rows never need a
+// host-side gather or one copy-engine request per row.  Two kernels:
+//
+// mode 0, gather_tma_kernel: each CTA is one warp that moves tiles of R
+//   consecutive selected rows of one (request, KV head).  Its lanes issue one
+//   bulk copy (cp.async.bulk, executed by the SM's tensor-memory-access unit)
+//   per K row and per V row, from host memory into a shared-memory stage; the
+//   stage completes on an mbarrier and is written to the scratch buffer with
+//   two contiguous bulk stores.  Several stages stay in flight per CTA.  The
+//   load/store pipeline is never blocked on the long host-link latency, which
+//   keeps the concurrent scoring kernel at speed.
+//
+// mode 1, gather_lsu_kernel: every thread keeps kInFlight 16-byte loads from
+//   host memory outstanding (consecutive threads read consecutive 16-byte
+//   pieces of a row).  Kept as the plain reference design.
 #include "dd_internal.cuh"
+
+// Grid of the bulk-copy gather, in percent of the SM count.
+#ifndef DD_GATHER_GRID_PCT
+#define DD_GATHER_GRID_PCT 200
+#endif
 
 namespace dd {
 namespace {
 
-constexpr int kGatherThreads = 256;
+__device__ unsigned int g_gather_status = 0;
+
+// ------------------------------------------------------------ mode 0 (TMA)
+constexpr int kTileBytes = 8192;  // per tensor per stage
+constexpr int kTmaStages = 4;
+constexpr size_t kTmaSmem = (size_t)2 * kTmaStages * kTileBytes + kTmaStages * sizeof(uint64_t);
+
+template <int RB>  // bytes per row
+__global__ void __launch_bounds__(32)
+    gather_tma_kernel(const unsigned char* __restrict__ k_host,
+                      const unsigned char* __restrict__ v_host, const int32_t* __restrict__ idx,
+                      unsigned char* __restrict__ k_buf, unsigned char* __restrict__ v_buf, int n,
+                      int k, int units) {
+  constexpr int R = kTileBytes / RB;  // rows per tile
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring_k = smem;
+  unsigned char* ring_v = smem + (size_t)kTmaStages * kTileBytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)2 * kTmaStages * kTileBytes);
+  const int lane = threadIdx.x;
+  const int tiles_per_unit = (k + R - 1) / R;
+  const int n_tiles = units * tiles_per_unit;
+
+  if (lane == 0) {
+    for (int s = 0; s < kTmaStages; ++s) mbar_init(&full[s], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+
+  // Issue the row copies of `tile` into stage s.
+  auto issue = [&](int tile, int s) {
+    const int u = tile / tiles_per_unit, i0 = (tile - u * tiles_per_unit) * R;
+    const int nr = min(R, k - i0);
+    if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * nr * RB));
+    __syncwarp();
+    for (int r = lane; r < nr; r += 32) {
+      const int j = min(max(__ldg(idx + (size_t)u * k + i0 + r), 0), n - 1);  // never outside
+      const size_t src = ((size_t)u * n + j) * RB;
+      bulk_load(ring_k + (size_t)s * kTileBytes + (size_t)r * RB, k_host + src, RB, &full[s]);
+      bulk_load(ring_v + (size_t)s * kTileBytes + (size_t)r * RB, v_host + src, RB, &full[s]);
+    }
+  };
+
+  for (int p = 0; p < kTmaStages; ++p) {
+    const int t = blockIdx.x + p * gridDim.x;
+    if (t < n_tiles) issue(t, p);
+  }
+  bool ok = true;
+  int it = 0;
+  for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+    const int s = it % kTmaStages;
+    if (!mbar_wait(&full[s], (it / kTmaStages) & 1)) {
+      ok = false;
+      break;
+    }
+    if (lane == 0) {
+      const int u = t / tiles_per_unit, i0 = (t - u * tiles_per_unit) * R;
+      const int nr = min(R, k - i0);
+      const size_t dst = ((size_t)u * k + i0) * RB;
+      bulk_store(k_buf + dst, ring_k + (size_t)s * kTileBytes, (uint32_t)(nr * RB));
+      bulk_store(v_buf + dst, ring_v + (size_t)s * kTileBytes, (uint32_t)(nr * RB));
+      bulk_commit();
+      bulk_wait_read_all();  // the stage may be refilled once the stores have read it
+    }
+    __syncwarp();
+    const int nt = t + kTmaStages * gridDim.x;
+    if (nt < n_tiles) issue(nt, s);
+  }
+  if (!ok) {
+    if (lane == 0) atomicOr(&g_gather_status, 1u);
+    // let the copies still in flight land before the CTA exits
+    for (int s = 0; s < kTmaStages; ++s) {
+      mbar_wait(&full[s], 0);
+      mbar_wait(&full[s], 1);
+    }
+  }
+  if (lane == 0) bulk_wait_all();
+}
+
+template <int RB>
+cudaError_t launch_tma(const Dims& d, const void* kh, const void* vh, const int32_t* idx,
+                       void* kb, void* vb, cudaStream_t st) {
+  static unsigned long long prepared = 0;
+  cudaError_t e = prepare_kernel(gather_tma_kernel<RB>, &prepared, (int)kTmaSmem);
+  if (e != cudaSuccess) return e;
+  constexpr int R = kTileBytes / RB;
+  const long long tiles = (long long)d.U * ((d.k + R - 1) / R);
+  long long grid = (long long)sm_count() * DD_GATHER_GRID_PCT / 100;
+  if (grid > tiles) grid = tiles;
+  if (grid < 1) grid = 1;
+  gather_tma_kernel<RB><<<(unsigned)grid, 32, kTmaSmem, st>>>(
+      static_cast<const unsigned char*>(kh), static_cast<const unsigned char*>(vh), idx,
+      static_cast<unsigned char*>(kb), static_cast<unsigned char*>(vb), d.n, d.k, d.U);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ mode 1 (LSU)
+constexpr int kLsuThreads = 256;
 constexpr int kInFlight = 8;
 
 template <int CPR>  // 16-byte pieces per row
-__global__ void __launch_bounds__(kGatherThreads)
-    gather_kernel(const uint4* __restrict__ k_host, const uint4* __restrict__ v_host,
-                  const int32_t* __restrict__ idx, uint4* __restrict__ k_buf,
-                  uint4* __restrict__ v_buf, int n, int k, long long rows) {
+__global__ void __launch_bounds__(kLsuThreads)
+    gather_lsu_kernel(const uint4* __restrict__ k_host, const uint4* __restrict__ v_host,
+                      const int32_t* __restrict__ idx, uint4* __restrict__ k_buf,
+                      uint4* __restrict__ v_buf, int n, int k, long long rows) {
   // Piece p of the flattened work list: row r = p / (2 CPR), tensor t (K or
   // V) = (p / CPR) & 1, part = p % CPR.
   const long long total = rows * 2 * CPR;
-  const long long stride = (long long)gridDim.x * kGatherThreads;
-  for (long long p0 = (long long)blockIdx.x * kGatherThreads + threadIdx.x; p0 < total;
+  const long long stride = (long long)gridDim.x * kLsuThreads;
+  for (long long p0 = (long long)blockIdx.x * kLsuThreads + threadIdx.x; p0 < total;
        p0 += stride * kInFlight) {
     uint4 v[kInFlight];
     long long dst[kInFlight];
@@ -59,15 +168,18 @@ __global__ void __launch_bounds__(kGatherThreads)
 }
 
 template <int CPR>
-cudaError_t launch_typed(const Dims& d, const void* kh, const void* vh, const int32_t* idx,
-                         void* kb, void* vb, cudaStream_t st) {
+cudaError_t launch_lsu(const Dims& d, const void* kh, const void* vh, const int32_t* idx,
+                       void* kb, void* vb, cudaStream_t st) {
+  static unsigned long long prepared = 0;
+  cudaError_t e = prepare_kernel(gather_lsu_kernel<CPR>, &prepared, 0);
+  if (e != cudaSuccess) return e;
   const long long rows = (long long)d.U * d.k;
-  const long long work = (rows * 2 * CPR + (long long)kGatherThreads * kInFlight - 1) /
-                         ((long long)kGatherThreads * kInFlight);
+  const long long work = (rows * 2 * CPR + (long long)kLsuThreads * kInFlight - 1) /
+                         ((long long)kLsuThreads * kInFlight);
   long long grid = sm_count();  // one CTA per SM at most
   if (grid > work) grid = work;
   if (grid < 1) grid = 1;
-  gather_kernel<CPR><<<(unsigned)grid, kGatherThreads, 0, st>>>(
+  gather_lsu_kernel<CPR><<<(unsigned)grid, kLsuThreads, 0, st>>>(
       static_cast<const uint4*>(kh), static_cast<const uint4*>(vh), idx,
       static_cast<uint4*>(kb), static_cast<uint4*>(vb), d.n, d.k, rows);
   return cudaGetLastError();
@@ -76,13 +188,30 @@ cudaError_t launch_typed(const Dims& d, const void* kh, const void* vh, const in
 }  // namespace
 
 cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
-                          const int32_t* idx, void* k_buf, void* v_buf, cudaStream_t st) {
-  switch (d.d * d.elt / 16) {
-    case 8: return launch_typed<8>(d, k_host, v_host, idx, k_buf, v_buf, st);
-    case 16: return launch_typed<16>(d, k_host, v_host, idx, k_buf, v_buf, st);
-    case 32: return launch_typed<32>(d, k_host, v_host, idx, k_buf, v_buf, st);
+                          const int32_t* idx, void* k_buf, void* v_buf, int mode,
+                          cudaStream_t st) {
+  const int rb = d.d * d.elt;
+  if (mode == 0) {
+    switch (rb) {
+      case 128: return launch_tma<128>(d, k_host, v_host, idx, k_buf, v_buf, st);
+      case 256: return launch_tma<256>(d, k_host, v_host, idx, k_buf, v_buf, st);
+      case 512: return launch_tma<512>(d, k_host, v_host, idx, k_buf, v_buf, st);
+    }
+  } else if (mode == 1) {
+    switch (rb / 16) {
+      case 8: return launch_lsu<8>(d, k_host, v_host, idx, k_buf, v_buf, st);
+      case 16: return launch_lsu<16>(d, k_host, v_host, idx, k_buf, v_buf, st);
+      case 32: return launch_lsu<32>(d, k_host, v_host, idx, k_buf, v_buf, st);
+    }
   }
   return cudaErrorInvalidValue;
+}
+
+unsigned int take_gather_status() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_gather_status, sizeof v) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_gather_status, &zero, sizeof zero);
+  return v;
 }
 
 }  // namespace dd

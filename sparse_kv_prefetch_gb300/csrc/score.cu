@@ -6,10 +6,15 @@
 // being processed and the key cache.)
 //
 // The kernel is HBM-bound: every K row is read exactly once, 2 flops per
-// element.  Each group of LPR lanes owns one K row per load (LPR x 16 bytes =
-// d elements), a lane keeps U rows in flight, and the lane group reduces the
-// partial dot products with xor-shuffles.  All query heads of a GQA group are
-// scored from the same K load.
+// element.  Each CTA owns one chunk of positions of one (request, KV head)
+// unit.  One producer warp streams the chunk through a ring of shared-memory
+// stages with bulk copies (cp.async.bulk on the tensor-memory-access unit,
+// completion on an mbarrier), so many bytes are in flight per SM without
+// occupying the load/store pipeline or registers.  Eight consumer warps read
+// each stage: LPR lanes share one K row (16 bytes each), the partial dot
+// products are reduced with xor-shuffles, and the lane that owns a row
+// writes its logit and folds it into a running (max, sum of exp).  All query
+// heads of a GQA group are scored from the same K row.
 #include <math.h>
 
 #include "dd_internal.cuh"
@@ -17,50 +22,61 @@
 namespace dd {
 namespace {
 
-constexpr int kScoreThreads = 256;
-constexpr int kScoreWarps = kScoreThreads / 32;
-constexpr int kRowsInFlight = 8;  // U: rows per lane group per iteration
-constexpr int kItersPerChunk = 8;
+constexpr int kConsumerWarps = 8;
+constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kStageBytes = 16384;
+constexpr int kStages = 4;
+constexpr int kStagesPerChunk = 16;  // 256 KiB of K per CTA
+
+// Set when a bounded wait gave up (read and cleared by dd_check_device).
+__device__ unsigned int g_score_status = 0;
 
 template <typename T, int D>
 struct ScoreGeom {
-  static constexpr int kVec = Elem<T>::kVec;
-  static constexpr int kLpr = D / kVec;          // lanes per row
-  static constexpr int kRpw = 32 / kLpr;         // rows per warp per load
-  static constexpr int kGroups = kScoreWarps * kRpw;
-  static constexpr int kRowsIt = kGroups * kRowsInFlight;
-  static constexpr int kChunk = kRowsIt * kItersPerChunk;
-  static_assert(kLpr >= kRowsInFlight && kLpr <= 32, "unsupported row width");
+  static constexpr int kVec = Elem<T>::kVec;            // elements per 16 bytes
+  static constexpr int kRowBytes = D * (int)sizeof(T);  // 128, 256 or 512
+  static constexpr int kLpr = D / kVec;                 // lanes per row
+  static constexpr int kRpw = 32 / kLpr;                // rows per warp per pass
+  static constexpr int kGroups = kConsumerWarps * kRpw; // row groups per CTA
+  static constexpr int kStageRows = kStageBytes / kRowBytes;
+  static constexpr int kRowsPerGroup = kStageRows / kGroups;
+  static constexpr int kChunk = kStageRows * kStagesPerChunk;
+  static_assert(kLpr >= kRowsPerGroup && kLpr <= 32, "unsupported row width");
+  static_assert(kStageRows % kGroups == 0, "stage must hold whole row groups");
 };
+
+constexpr size_t kScoreSmem = (size_t)kStages * kStageBytes + 2 * kStages * sizeof(uint64_t);
 
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kScoreThreads)
-    score_kernel(const uint4* __restrict__ q_spec, const uint4* __restrict__ K,
+    score_kernel(const uint4* __restrict__ q_spec, const unsigned char* __restrict__ K,
                  float* __restrict__ logits, float2* __restrict__ part, int n, int ldn, int Hq,
                  int Hkv, int nchunks, float scale) {
   using Geo = ScoreGeom<T, D>;
-  constexpr int VEC = Geo::kVec, LPR = Geo::kLpr, RPW = Geo::kRpw;
-  constexpr int NG = Geo::kGroups, U = kRowsInFlight;
-  constexpr int V16 = D / VEC;  // 16-byte vectors per row (== LPR)
+  constexpr int VEC = Geo::kVec, LPR = Geo::kLpr, RPW = Geo::kRpw, NG = Geo::kGroups;
+  constexpr int SR = Geo::kStageRows, RPG = Geo::kRowsPerGroup, RB = Geo::kRowBytes;
+
+  extern __shared__ __align__(128) unsigned char smem[];
+  unsigned char* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
 
   const int item = blockIdx.x;
   const int u = item / nchunks, c = item - u * nchunks;
   const int b = u / Hkv, hk = u - b * Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int sub = lane % LPR;
-  const int grp = warp * RPW + lane / LPR;
-
-  // This lane's slice of each query head of the group, in fp32.
-  float qf[G][VEC];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4 v = ld_ro(q_spec + ((size_t)(b * Hq + hk * G + g)) * V16 + sub);
-    unpack(v, qf[g]);
-  }
-
-  const uint4* Ku = K + (size_t)u * n * V16;
   const int j_begin = c * Geo::kChunk;
   const int j_end = min(n, j_begin + Geo::kChunk);
+  const int n_stages = (j_end - j_begin + SR - 1) / SR;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kConsumerWarps);
+    }
+    mbar_fence_init();
+  }
+  __syncthreads();
 
   float m_run[G], l_run[G];
 #pragma unroll
@@ -68,55 +84,93 @@ __global__ void __launch_bounds__(kScoreThreads)
     m_run[g] = -INFINITY;
     l_run[g] = 0.f;
   }
+  bool ok = true;
+  const unsigned char* Ku = K + (size_t)u * n * RB;
 
-  for (int base = j_begin; base < j_end; base += Geo::kRowsIt) {
-    uint4 v[U];
-#pragma unroll
-    for (int i = 0; i < U; ++i) {
-      const int j = base + i * NG + grp;
-      v[i] = (j < j_end) ? ld_stream(Ku + (size_t)j * V16 + sub) : make_uint4(0, 0, 0, 0);
-    }
-    float acc[G][U];
-#pragma unroll
-    for (int i = 0; i < U; ++i) {
-      float kf[VEC];
-      unpack(v[i], kf);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float a = 0.f;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) a = fmaf(qf[g][e], kf[e], a);
-        acc[g][i] = a;
+  if (warp == kConsumerWarps) {
+    // Producer: one lane keeps up to kStages bulk copies in flight.
+    if (lane == 0) {
+      for (int t = 0; t < n_stages; ++t) {
+        const int s = t % kStages;
+        if (t >= kStages && !mbar_wait(&empty[s], ((t / kStages) - 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const int r0 = j_begin + t * SR;
+        const int nr = min(SR, j_end - r0);
+        mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * RB));
+        bulk_load(ring + (size_t)s * kStageBytes, Ku + (size_t)r0 * RB, (uint32_t)(nr * RB),
+                  &full[s]);
       }
     }
-    // Sum over the LPR lanes of each row group.
+  } else {
+    const int sub = lane % LPR;
+    const int grp = warp * RPW + lane / LPR;
+    float qf[G][VEC];
 #pragma unroll
-    for (int off = LPR / 2; off > 0; off >>= 1)
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int i = 0; i < U; ++i) acc[g][i] += __shfl_xor_sync(0xffffffffu, acc[g][i], off);
+    for (int g = 0; g < G; ++g)
+      unpack(ld_ro(q_spec + ((size_t)(b * Hq + hk * G + g)) * LPR + sub), qf[g]);
 
-    // Lane `sub` of the group owns row i == sub.
-    const int j = base + sub * NG + grp;
-    if (sub < U && j < j_end) {
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float s = 0.f;
-#pragma unroll
-        for (int i = 0; i < U; ++i)
-          if (i == sub) s = acc[g][i];
-        s *= scale;
-        logits[(size_t)(b * Hq + hk * G + g) * ldn + j] = s;
-        const float m_new = fmaxf(m_run[g], s);
-        l_run[g] = l_run[g] * __expf(m_run[g] - m_new) + __expf(s - m_new);
-        m_run[g] = m_new;
+    for (int t = 0; t < n_stages; ++t) {
+      const int s = t % kStages;
+      if (!mbar_wait(&full[s], (t / kStages) & 1)) {
+        ok = false;
+        break;
       }
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * kStageBytes);
+      const int r0 = j_begin + t * SR;
+      // Row (i * NG + grp) of the stage, for i < RPG, belongs to this lane group.
+      float acc[G][RPG];
+#pragma unroll
+      for (int i = 0; i < RPG; ++i) {
+        float kf[VEC];
+        unpack(st[(size_t)(i * NG + grp) * LPR + sub], kf);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float a = 0.f;
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) a = fmaf(qf[g][e], kf[e], a);
+          acc[g][i] = a;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+#pragma unroll
+      for (int off = LPR / 2; off > 0; off >>= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int i = 0; i < RPG; ++i) acc[g][i] += __shfl_xor_sync(0xffffffffu, acc[g][i], off);
+      // Lane `sub` of the group owns row i == sub.
+      const int j = r0 + sub * NG + grp;
+      if (sub < RPG && j < j_end) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+          float sv = 0.f;
+#pragma unroll
+          for (int i = 0; i < RPG; ++i)
+            if (i == sub) sv = acc[g][i];
+          sv *= scale;
+          logits[(size_t)(b * Hq + hk * G + g) * ldn + j] = sv;
+          const float m_new = fmaxf(m_run[g], sv);
+          l_run[g] = l_run[g] * __expf(m_run[g] - m_new) + __expf(sv - m_new);
+          m_run[g] = m_new;
+        }
+      }
+    }
+  }
+  if (!ok) atomicOr(&g_score_status, 1u);
+  __syncthreads();
+  if (!ok && threadIdx.x == 0) {
+    // A wait gave up: let the copies still in flight land before exiting.
+    for (int s = 0; s < kStages; ++s) {
+      mbar_wait(&full[s], 0);
+      mbar_wait(&full[s], 1);
     }
   }
 
   // CTA-wide merge of the (max, sum) pairs of each head.
-  __shared__ float2 red[G][kScoreWarps];
+  __shared__ float2 red[G][kConsumerWarps + 1];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
     float2 p = make_float2(m_run[g], l_run[g]);
@@ -134,7 +188,7 @@ __global__ void __launch_bounds__(kScoreThreads)
     const int g = threadIdx.x;
     float2 p = red[g][0];
 #pragma unroll
-    for (int w = 1; w < kScoreWarps; ++w) p = lse_merge(p, red[g][w]);
+    for (int w = 1; w <= kConsumerWarps; ++w) p = lse_merge(p, red[g][w]);
     part[(size_t)(u * G + g) * nchunks + c] = p;
   }
 }
@@ -142,11 +196,14 @@ __global__ void __launch_bounds__(kScoreThreads)
 template <typename T, int D, int G>
 cudaError_t launch_typed(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
                          float2* part, cudaStream_t st) {
+  static unsigned long long prepared = 0;
+  cudaError_t e = prepare_kernel(score_kernel<T, D, G>, &prepared, (int)kScoreSmem);
+  if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)d.d);
   const unsigned grid = (unsigned)d.U * (unsigned)d.nchunks;
-  score_kernel<T, D, G><<<grid, kScoreThreads, 0, st>>>(
-      static_cast<const uint4*>(q_spec), static_cast<const uint4*>(k_dev), logits, part, d.n,
-      d.ldn, d.Hq, d.Hkv, d.nchunks, scale);
+  score_kernel<T, D, G><<<grid, kScoreThreads, kScoreSmem, st>>>(
+      static_cast<const uint4*>(q_spec), static_cast<const unsigned char*>(k_dev), logits, part,
+      d.n, d.ldn, d.Hq, d.Hkv, d.nchunks, scale);
   return cudaGetLastError();
 }
 
@@ -187,6 +244,13 @@ cudaError_t launch_score(const Dims& d, const void* q_spec, const void* k_dev, f
     if (d.d == 128) return launch_g<float, 128>(d, q_spec, k_dev, logits, part, st);
   }
   return cudaErrorInvalidValue;
+}
+
+unsigned int take_score_status() {
+  unsigned int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_score_status, sizeof v) != cudaSuccess) return 0;
+  if (v) cudaMemcpyToSymbol(g_score_status, &zero, sizeof zero);
+  return v;
 }
 
 }  // namespace dd

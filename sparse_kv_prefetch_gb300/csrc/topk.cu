@@ -337,18 +337,9 @@ __global__ void __launch_bounds__(kTkThreads, 1)
 template <int G>
 cudaError_t launch_typed(const Dims& d, const float* logits, const float2* part, int32_t* idx,
                          float* sel, float* lse, cudaStream_t st) {
-  // Opt in to more than 48 KB of dynamic shared memory, once per device.
-  static unsigned long long attr_done = 0;
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  static unsigned long long prepared = 0;
+  cudaError_t e = prepare_kernel(topk_kernel<G>, &prepared, (int)sizeof(TkSmem));
   if (e != cudaSuccess) return e;
-  const unsigned long long bit = 1ull << (dev & 63);
-  if (!(__atomic_load_n(&attr_done, __ATOMIC_ACQUIRE) & bit)) {
-    e = cudaFuncSetAttribute(topk_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)sizeof(TkSmem));
-    if (e != cudaSuccess) return e;
-    __atomic_fetch_or(&attr_done, bit, __ATOMIC_ACQ_REL);
-  }
   topk_kernel<G><<<d.U, kTkThreads, sizeof(TkSmem), st>>>(logits, part, idx, sel, lse, d.Hq, d.Hkv,
                                                           d.ldn, d.span, d.k, d.nchunks);
   return cudaGetLastError();

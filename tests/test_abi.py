@@ -84,8 +84,8 @@ def test_null_and_misaligned_pointers_rejected():
     st = lib.dd_sparse_decode_attn(ctypes.byref(shp), 16, 16, 16, 16, None, 16, 16, 1 << 30,
                                    None)  # W > 0 needs the window V
     assert st == dd.DD_ERR_INVALID_ARG
-    st = lib.dd_gather_h2d(ctypes.byref(shp), 16, 16, 16, 16, 16, 1, None)
-    assert st == dd.DD_ERR_UNSUPPORTED  # only the zero-copy mode exists
+    st = lib.dd_gather_h2d(ctypes.byref(shp), 16, 16, 16, 16, 16, 2, None)
+    assert st == dd.DD_ERR_UNSUPPORTED  # modes 0 (bulk copy) and 1 (load/store) only
     st = lib.dd_score_topk(ctypes.byref(shp), 16, 16, 16, 16, None, 16, 1024, None)
     assert st == dd.DD_ERR_INVALID_ARG  # workspace too small
     assert lib.dd_decode_step(None, None, 0, None, None, 0) == dd.DD_ERR_INVALID_ARG

@@ -62,6 +62,13 @@ def test_layer_small(name):
             b, hk = divmod(u, w.n_kv_heads)
             assert set(s.planted[b, hk, :w.n_planted].tolist()) <= set(idx[u].tolist())
     check_gather(w, s, idx, o.k_buf, o.v_buf, range(w.units))
+    # the load/store gather (mode 1) moves the same bytes as the bulk-copy one
+    kb1, vb1 = torch.empty_like(o.k_buf), torch.empty_like(o.v_buf)
+    dd.gather_h2d(dd_shape(w), s.K_h, s.V_h, o.idx, kb1, vb1, mode=1)
+    torch.cuda.synchronize()
+    assert torch.equal(kb1.view(torch.uint8), o.k_buf.view(torch.uint8))
+    assert torch.equal(vb1.view(torch.uint8), o.v_buf.view(torch.uint8))
+    dd.check_device()
 
 
 @pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
@@ -147,12 +154,16 @@ def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
     ctx.decode_step(_layers(w, slots, outs_a, L), compute=compute, copy=copy, timing=True)
     t = ctx.timings()
     ctx.decode_step(_layers(w, slots, outs_b, L), compute=compute, copy=None)
+    outs_c = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
+    ctx.decode_step(_layers(w, slots, outs_c, L), compute=compute, copy=copy, late_gather=True)
     torch.cuda.synchronize()
     for l in range(L):
         assert torch.equal(outs_a[l], outs_b[l]), f"layer {l}: overlapped != serial"
+        assert torch.equal(outs_c[l], outs_b[l]), f"layer {l}: late gather != serial"
         assert torch.equal(outs_a[l], ref[l % D]), f"layer {l}: step != per-layer calls"
     assert t["n_layers"] == L and t["launches"] == L * 5
     assert t["step_ms"] > 0 and t["score_ms"] > 0 and t["gather_ms"] > 0
+    dd.check_device()
     ctx.close()
 
 
