@@ -35,6 +35,11 @@ import synth  # noqa: E402
 METRIC = "sparse-decode layer-steps/s; scoring HBM GB/s; gather host-link GB/s"
 UNIT = "layer-steps/s"
 FALLBACK_HBM_GBS = 6800.0
+# DRAM read + write bytes of one score_kernel launch, from the ncu capture in
+# profiles/score_kernel_7b32k-batch2.md (batch 2: 546.75 MB for 64 units),
+# scaled by units to the 7B-32K layer (256 units); traffic grows with the
+# units processed.  Keyed by workload; None where no capture exists.
+SCORE_TRAFFIC_BYTES = {"c2-7b-32k": 546.75e6 * 256 / 64}
 
 
 def parse():
@@ -46,6 +51,10 @@ def parse():
     p.add_argument("--workload", default=synth.C2.name, choices=list(synth.WORKLOADS))
     p.add_argument("--profile-case", action="store_true",
                    help="small case for ncu captures: batch 2, 2 layers, 1 slot")
+    p.add_argument("--gather-mode", type=int, default=0, choices=[0, 1],
+                   help="0: bulk-copy gather, 1: load/store gather")
+    p.add_argument("--host-alloc", default="pinned", choices=["huge", "pinned"],
+                   help="host KV store: dd_host_alloc huge pages, or torch pinned memory")
     p.add_argument("--late-gather", type=int, default=0,
                    help="1: start each layer's gather after the previous attention")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -139,6 +148,17 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def anon_huge_bytes():
+    """Bytes of this process's memory backed by transparent huge pages."""
+    try:
+        for line in open("/proc/self/smaps_rollup"):
+            if line.startswith("AnonHugePages:"):
+                return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    return None
+
+
 def measured_hbm_peak():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -187,7 +207,9 @@ def config_of(w, args):
             "head_dim": w.head_dim, "ctx_len": w.ctx_len, "top_k": w.top_k, "window": w.window,
             "l2": "inputs larger than L2 (K of one layer is %.0f MiB; 129 MB L2)"
                   % (w.k_bytes() / 2**20),
-            "parallelism": f"replicas x{args.gpus} (independent requests per GPU)"}
+            "parallelism": f"replicas x{args.gpus} (independent requests per GPU)",
+            "gather_mode": ["bulk_copy", "load_store"][args.gather_mode],
+            "host_store": args.host_alloc, "late_gather": bool(args.late_gather)}
 
 
 def run_reference(args, rank, world):
@@ -226,8 +248,18 @@ def run_ours(args, rank, world):
     D, L = w.n_slots, w.n_layers
 
     # Host store (pinned) and the device-resident key cache, per layer slot.
-    K_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
-    V_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
+    huge0 = anon_huge_bytes()
+    # Pinned memory from torch by default.  dd_host_alloc's huge-page store
+    # made the gather faster in most runs on GB300, but the bulk-copy gather
+    # over it collapsed transiently in some runs.
+    if args.host_alloc == "huge":  # huge-page, page-locked host store
+        K_h = dd.host_empty((D, B, Hkv, n, d), dt)
+        V_h = dd.host_empty((D, B, Hkv, n, d), dt)
+    else:
+        K_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
+        V_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
+    store_bytes = 2 * K_h.numel() * K_h.element_size()
+    huge_frac = (anon_huge_bytes() - huge0) / store_bytes if huge0 is not None else None
     qs_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
     q_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
     t_gen = time.perf_counter()
@@ -292,7 +324,7 @@ def run_ours(args, rank, world):
 
     def step(copy_stream, timing=True):
         ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
-                        late_gather=args.late_gather)
+                        late_gather=args.late_gather, gather_mode=args.gather_mode)
         return ctx.timings() if timing else None
 
     compute.wait_stream(torch.cuda.current_stream())
@@ -341,7 +373,8 @@ def run_ours(args, rank, world):
         with torch.cuda.stream(compute):
             qs_l.copy_(qs_src, non_blocking=True)
             q_l.copy_(q_src, non_blocking=True)
-        ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=args.late_gather)
+        ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=args.late_gather,
+                        gather_mode=args.gather_mode)
         with torch.cuda.stream(compute):
             out_h.copy_(outs, non_blocking=True)
     for _ in range(2):
@@ -409,7 +442,9 @@ def run_ours(args, rank, world):
                                                 "attn_ms")},
         "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": score_gbs / peak, "traffic": None,
+                     "frac": score_gbs / peak,
+                     "traffic": (None if args.profile_case
+                                 else SCORE_TRAFFIC_BYTES.get(w.name)),
                      "algorithmic_bytes_per_launch": k_bytes},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT,
@@ -419,6 +454,8 @@ def run_ours(args, rank, world):
         "gpu_launches": launches,
         "clocks": clk,
         "setup_s": {"generate": t_gen},
+        "host_store": {"bytes": store_bytes, "huge_page_bytes": dd.host_page_bytes(),
+                       "huge_page_fraction": huge_frac},
         "ctx_device_bytes": ctx.device_bytes,
     }
     ctx.close()

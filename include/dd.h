@@ -104,6 +104,32 @@ int dd_version(void);
 dd_status dd_check_device(void);
 
 /*
+ * Host KV store allocation.  The GPU reads the host store through the host's
+ * page tables.  On a Grace host with 64 KiB base pages every scattered row of
+ * a cold gather needs its own page translation (about 4 us each), and the
+ * thousands in flight also slow the other kernels' memory requests.  Huge
+ * pages cut the translations to a handful per layer.  dd_host_alloc maps
+ * `bytes` (rounded up to whole huge pages) of anonymous memory aligned to the
+ * host's huge-page size, asks for transparent huge pages (madvise), faults it
+ * in from the CPU (several threads; the pages read as zero), and page-locks
+ * and maps it for the GPU (cudaHostRegister).  The caller owns the memory and
+ * releases it with dd_host_free.  Returns DD_ERR_OOM if the mapping fails and
+ * DD_ERR_CUDA if registration fails.  Any page-locked memory works with the
+ * gather.
+ * Measured on GB300 with 512 MiB huge pages, on the 7B-32K workload (8 layer
+ * slots cycled): most runs gathered at warm-translation speed, but in some
+ * runs the bulk-copy gather (mode 0) over such a store collapsed for a while,
+ * so the benchmark keeps plain page-locked memory as its default.
+ */
+dd_status dd_host_alloc(size_t bytes, void** out);
+/* Unregister and unmap a region from dd_host_alloc (NULL is a no-op);
+ * DD_ERR_INVALID_ARG for any other pointer. */
+dd_status dd_host_free(void* p);
+/* The host huge-page size the allocator and the gather's translation
+ * prefetch use (transparent-huge-page size, else 2 MiB). */
+size_t dd_host_page_bytes(void);
+
+/*
  * Bytes of device workspace that dd_score_topk and dd_sparse_decode_attn need
  * for this shape (fp32 logits [B][H_q][round_up(n,4)], per-chunk softmax
  * partials and split-k attention partials, each 256-byte aligned).
@@ -138,6 +164,9 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
  *                   outside that range is clamped into it on the device, so
  *                   the kernel never reads outside the store
  *   k_buf, v_buf    device [B][H_kv][k][d]
+ *   Before the copy, one warp reads a word per huge page of the two host
+ *   regions so their address translations are resolved once (a second, tiny
+ *   kernel on the same stream).
  *   mode            0 = bulk-copy gather: one-warp CTAs issue one
  *                       cp.async.bulk per row into shared memory and write
  *                       tiles back with bulk stores (used by dd_decode_step);
@@ -223,8 +252,10 @@ size_t dd_ctx_device_bytes(const dd_ctx* ctx);
 
 enum {
   DD_STEP_TIMING = 1,     /* record per-phase CUDA events; read with dd_ctx_timings */
-  DD_STEP_LATE_GATHER = 2 /* start the gather of layer l+1 after the attention of
-                             layer l (it then overlaps the scoring of layer l+2) */
+  DD_STEP_LATE_GATHER = 2, /* start the gather of layer l+1 after the attention of
+                              layer l (it then overlaps the scoring of layer l+2) */
+  DD_STEP_GATHER_LSU = 4   /* gather with dd_gather_h2d mode 1 (load/store)
+                              instead of mode 0 (bulk copy) */
 };
 
 /*

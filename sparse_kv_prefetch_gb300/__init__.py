@@ -24,6 +24,7 @@ DD_OK, DD_ERR_INVALID_ARG, DD_ERR_UNSUPPORTED, DD_ERR_OOM, DD_ERR_CUDA, DD_ERR_T
 DD_F32, DD_BF16 = 0, 1
 DD_STEP_TIMING = 1
 DD_STEP_LATE_GATHER = 2
+DD_STEP_GATHER_LSU = 4
 
 
 class DDError(RuntimeError):
@@ -82,6 +83,9 @@ def _lib():
             "dd_status_string": ([ctypes.c_int], ctypes.c_char_p),
             "dd_version": ([], ctypes.c_int),
             "dd_check_device": ([], ctypes.c_int),
+            "dd_host_alloc": ([ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
+            "dd_host_free": ([ctypes.c_void_p], ctypes.c_int),
+            "dd_host_page_bytes": ([], ctypes.c_size_t),
             "dd_workspace_size": ([S, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
             "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dd_gather_h2d": ([S, P, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
@@ -147,6 +151,29 @@ def _stream(s) -> Optional[int]:
 
 def version() -> int:
     return _lib().dd_version()
+
+
+def host_empty(shape, dtype):
+    """An uninitialised CPU tensor in a huge-page, page-locked host region from
+    dd_host_alloc (the recommended host KV store); freed with dd_host_free when
+    the tensor and all its views are gone."""
+    import weakref
+
+    import torch
+    numel = 1
+    for s_ in shape:
+        numel *= int(s_)
+    nbytes = max(1, numel * torch.empty((), dtype=dtype).element_size())
+    p = ctypes.c_void_p()
+    _check(_lib().dd_host_alloc(nbytes, ctypes.byref(p)), "dd_host_alloc")
+    buf = (ctypes.c_char * nbytes).from_address(p.value)
+    weakref.finalize(buf, _lib().dd_host_free, ctypes.c_void_p(p.value))
+    t = torch.frombuffer(buf, dtype=torch.uint8, count=nbytes)
+    return t.view(dtype)[:numel].view(*shape) if numel else t.view(dtype)[:0].view(*shape)
+
+
+def host_page_bytes() -> int:
+    return _lib().dd_host_page_bytes()
 
 
 def check_device():
@@ -246,12 +273,13 @@ class Ctx:
         return arr
 
     def decode_step(self, layers, compute=None, copy=None, timing: bool = False,
-                    late_gather: bool = False):
+                    late_gather: bool = False, gather_mode: int = 0):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
-        flags = (DD_STEP_TIMING if timing else 0) | (DD_STEP_LATE_GATHER if late_gather else 0)
+        flags = ((DD_STEP_TIMING if timing else 0) | (DD_STEP_LATE_GATHER if late_gather else 0)
+                 | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0))
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 

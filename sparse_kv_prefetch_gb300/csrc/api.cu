@@ -9,9 +9,21 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <sys/mman.h>
+
+#include <algorithm>
+
+#include <cstdio>
 #include <initializer_list>
+#include <map>
+#include <mutex>
 #include <new>
+#include <thread>
 #include <vector>
+
+#ifndef DD_HOST_PREFAULT
+#define DD_HOST_PREFAULT 1
+#endif
 
 #include "dd_internal.cuh"
 
@@ -70,6 +82,20 @@ dd_status resolve(const dd_shape* s, Dims* o) {
   if ((long long)d.U * d.k > 0x7FFFFFFFLL) return DD_ERR_UNSUPPORTED;
   *o = d;
   return DD_OK;
+}
+
+size_t host_page_bytes() {
+  static size_t cached = 0;
+  if (cached) return cached;
+  size_t v = 0;
+  if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
+    unsigned long long x = 0;
+    if (std::fscanf(f, "%llu", &x) == 1) v = (size_t)x;
+    std::fclose(f);
+  }
+  if (v < 4096 || (v & (v - 1))) v = (size_t)2 << 20;
+  cached = v;
+  return v;
 }
 
 WsLayout ws_layout(const Dims& d) {
@@ -142,6 +168,77 @@ const char* dd_status_string(int s) {
 }
 
 int dd_version(void) { return DD_VERSION; }
+
+// ------------------------------------------------------------ host store
+
+namespace {
+std::mutex g_host_mu;
+std::map<void*, size_t> g_host_regions;  // dd_host_alloc base -> mapped bytes
+}  // namespace
+
+dd_status dd_host_alloc(size_t bytes, void** out) {
+  if (!out || bytes == 0) return DD_ERR_INVALID_ARG;
+  *out = nullptr;
+  const size_t page = host_page_bytes();
+  const size_t len = (bytes + page - 1) / page * page;
+  // Over-map by one huge page so the region can start on a huge-page boundary.
+  void* raw = mmap(nullptr, len + page, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
+  if (raw == MAP_FAILED) return DD_ERR_OOM;
+  const uintptr_t r = (uintptr_t)raw;
+  const uintptr_t base = (r + page - 1) / page * page;
+  if (base > r) munmap(raw, base - r);
+  const uintptr_t tail = base + len, raw_end = r + len + page;
+  if (raw_end > tail) munmap((void*)tail, raw_end - tail);
+  void* p = (void*)base;
+  madvise(p, len, MADV_HUGEPAGE);  // advisory: huge pages where the host allows them
+#if DD_HOST_PREFAULT
+  // Fault the region in from the CPU (one store per 64 KiB, several threads,
+  // each on its own huge pages) before registering it, so that the kernel
+  // backs it with huge pages at first touch.
+  {
+    const unsigned hw = std::thread::hardware_concurrency();
+    const size_t n_pages = len / page;
+    const unsigned n_thr = (unsigned)std::min<size_t>(n_pages, hw ? std::min(hw, 16u) : 4u);
+    auto fault = [&](unsigned t) {
+      for (size_t pg = t; pg < n_pages; pg += n_thr)
+        for (size_t off = 0; off < page; off += 65536)
+          static_cast<volatile unsigned char*>(p)[pg * page + off] = 0;
+    };
+    std::vector<std::thread> th;
+    for (unsigned t = 1; t < n_thr; ++t) th.emplace_back(fault, t);
+    fault(0);
+    for (auto& x : th) x.join();
+  }
+#endif
+  if (cudaHostRegister(p, len, cudaHostRegisterDefault) != cudaSuccess) {
+    cudaGetLastError();
+    munmap(p, len);
+    return DD_ERR_CUDA;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    g_host_regions[p] = len;
+  }
+  *out = p;
+  return DD_OK;
+}
+
+dd_status dd_host_free(void* p) {
+  if (!p) return DD_OK;
+  size_t len = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_host_mu);
+    auto it = g_host_regions.find(p);
+    if (it == g_host_regions.end()) return DD_ERR_INVALID_ARG;
+    len = it->second;
+    g_host_regions.erase(it);
+  }
+  const cudaError_t e = cudaHostUnregister(p);
+  munmap(p, len);
+  return e == cudaSuccess ? DD_OK : DD_ERR_CUDA;
+}
+
+size_t dd_host_page_bytes(void) { return host_page_bytes(); }
 
 dd_status dd_check_device(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return DD_ERR_CUDA;
@@ -361,6 +458,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     if (!all_device({io.q_spec, io.q, io.k_dev, io.v_win, io.out})) return DD_ERR_INVALID_ARG;
   }
   const bool timing = (flags & DD_STEP_TIMING) != 0;
+  const int gather_mode = (flags & DD_STEP_GATHER_LSU) ? 1 : 0;
   if (timing) {
     dd_status st = ensure_timing_events(c, n_layers);
     if (st != DD_OK) return st;
@@ -405,7 +503,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       if (e != cudaSuccess) return e;
     }
     if (timing) cudaEventRecord(T(l, PH_GATHER0), X);
-    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], 0, X);
+    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X);
     if (e != cudaSuccess) return e;
     if (timing) cudaEventRecord(T(l, PH_GATHER1), X);
     launches += kGatherLaunches;

@@ -66,6 +66,9 @@ __global__ void __launch_bounds__(kAttnThreads)
     return (r < k) ? v_buf + ((size_t)u * k + r) * V16 : v_win + ((size_t)u * W + (r - k)) * V16;
   };
 
+  // Both the K and the V rows of this lane are requested up front, so the
+  // softmax below does not wait for a second round trip to memory.
+  uint4 vv[IT];
   // Phase 1: logits of this split's rows.
   {
     uint4 kv[IT];
@@ -73,6 +76,11 @@ __global__ void __launch_bounds__(kAttnThreads)
     for (int i = 0; i < IT; ++i) {
       const int rl = i * NG + grp;
       kv[i] = (rl < nr) ? ld_ro(k_row(r0 + rl) + sub) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < IT; ++i) {
+      const int rl = i * NG + grp;
+      vv[i] = (rl < nr) ? ld_ro(v_row(r0 + rl) + sub) : make_uint4(0, 0, 0, 0);
     }
 #pragma unroll
     for (int i = 0; i < IT; ++i) {
@@ -124,12 +132,6 @@ __global__ void __launch_bounds__(kAttnThreads)
 #pragma unroll
     for (int e = 0; e < VEC; ++e) acc[g][e] = 0.f;
   {
-    uint4 vv[IT];
-#pragma unroll
-    for (int i = 0; i < IT; ++i) {
-      const int rl = i * NG + grp;
-      vv[i] = (rl < nr) ? ld_ro(v_row(r0 + rl) + sub) : make_uint4(0, 0, 0, 0);
-    }
 #pragma unroll
     for (int i = 0; i < IT; ++i) {
       const int rl = i * NG + grp;

@@ -45,7 +45,11 @@ cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const v
                         float2* part_ml, cudaStream_t st);
 
 // Number of kernels each launcher enqueues.
-constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 1, kAttnLaunches = 2;
+constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 2, kAttnLaunches = 2;
+
+// Huge-page size of the host (transparent huge pages), read once; 2 MiB if
+// the host does not report one.  Host stores from dd_host_alloc use it.
+size_t host_page_bytes();
 
 int sm_count();
 

@@ -32,6 +32,37 @@ namespace {
 
 __device__ unsigned int g_gather_status = 0;
 
+// ---------------------------------------------------- translation prefetch
+//
+// The GPU reaches host memory through the host's page tables.  When thousands
+// of gather requests first hit a page whose translation is not cached, every
+// one of them waits on the same translation, and the storm also delays the
+// other kernels' memory requests.  Before each gather one warp therefore reads
+// one word per huge page of the layer's K and V regions (at the region start
+// and at every page boundary inside it, so every read stays inside the
+// caller's buffer): each translation is then resolved once, and the gather
+// that follows runs at full speed.  With huge pages (dd_host_alloc) this is a
+// handful of reads per layer.
+__global__ void __launch_bounds__(32)
+    touch_pages_kernel(const unsigned char* __restrict__ k_host,
+                       const unsigned char* __restrict__ v_host, size_t bytes, size_t stride,
+                       unsigned int* __restrict__ sink) {
+  unsigned int acc = 0;
+  for (int t = 0; t < 2; ++t) {
+    const unsigned char* base = t ? v_host : k_host;
+    const uintptr_t start = (uintptr_t)base, end = start + bytes;
+    const uintptr_t first = (start / stride + 1) * stride;  // first page boundary after start
+    const size_t n_pages = end > first ? (end - first + stride - 1) / stride : 0;
+    for (size_t i = threadIdx.x; i <= n_pages; i += 32) {
+      const uintptr_t a = i == 0 ? start : first + (i - 1) * stride;
+      if (a < end) acc += *reinterpret_cast<const volatile unsigned int*>(a & ~(uintptr_t)3);
+    }
+  }
+  if (acc == 0x9E3779B9u) *sink = acc;  // keeps the reads; practically never taken
+}
+
+__device__ unsigned int g_touch_sink = 0;
+
 // ------------------------------------------------------------ mode 0 (TMA)
 constexpr int kTileBytes = 8192;  // per tensor per stage
 constexpr int kTmaStages = 4;
@@ -191,6 +222,23 @@ cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
                           const int32_t* idx, void* k_buf, void* v_buf, int mode,
                           cudaStream_t st) {
   const int rb = d.d * d.elt;
+  if (mode == 0 || mode == 1) {
+    static unsigned int* sinks[64] = {};  // device address of g_touch_sink, per device
+    int dev = 0;
+    cudaError_t e0 = cudaGetDevice(&dev);
+    if (e0 != cudaSuccess) return e0;
+    unsigned int*& sink = sinks[dev & 63];
+    if (!sink) {
+      e0 = cudaGetSymbolAddress(reinterpret_cast<void**>(&sink), g_touch_sink);
+      if (e0 != cudaSuccess) return e0;
+    }
+    const size_t bytes = (size_t)d.U * d.n * rb;
+    touch_pages_kernel<<<1, 32, 0, st>>>(static_cast<const unsigned char*>(k_host),
+                                         static_cast<const unsigned char*>(v_host), bytes,
+                                         host_page_bytes(), sink);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   if (mode == 0) {
     switch (rb) {
       case 128: return launch_tma<128>(d, k_host, v_host, idx, k_buf, v_buf, st);

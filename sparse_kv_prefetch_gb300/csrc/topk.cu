@@ -8,18 +8,22 @@
 // heads a[j] = sum over the group of exp(s_hj - LSE_h) in fp32.  LSE_h is
 // first merged from the scoring kernel's per-chunk (max, sum) pairs.
 //
-// Exact radix select on order-preserving 32-bit keys, one CTA per unit:
-//   pass A  histogram of key bits 31..21 over the unit (global reads);
-//           the bucket b1 that holds the k-th largest key is found by a
-//           block scan from the top;
-//   pass B  every key with top bits >= b1 is compacted, in position order,
-//           into a shared-memory list (typically a few thousand entries);
+// Exact radix select on order-preserving 32-bit keys, one CTA per unit.  Each
+// warp owns a contiguous segment of the positions, so position order is the
+// order (warp, position within the warp's segment):
+//   pass A  histogram of key bits 31..21 over the unit (global reads); the
+//           bucket b1 that holds the k-th largest key is found by a block
+//           scan from the top;
+//   pass B  every warp compacts the keys of its segment with top bits >= b1,
+//           in position order, into its own shared-memory list (ballots and
+//           shuffle scans only, no block barrier);
 //   refine  bits 20..10 and 9..0 of the threshold key T are resolved on the
-//           list with two more histograms;
-//   emit    one ordered scan over the list writes every key > T plus the
-//           first (lowest-position) k_rem keys equal to T.
-// If the list would overflow shared memory (very many near-equal scores),
-// the refine and emit steps run over global memory instead: same result.
+//           lists with two more histograms;
+//   emit    every key > T plus the first (lowest-position) k_rem keys equal
+//           to T are written; each warp places its entries after the counts of
+//           the warps before it.
+// If a warp's list would overflow (very many near-equal scores), the refine
+// and emit steps run over global memory instead: the same result.
 #include <math.h>
 
 #include "dd_internal.cuh"
@@ -27,16 +31,22 @@
 namespace dd {
 namespace {
 
-constexpr int kTkThreads = 1024;
+constexpr int kTkThreads = 512;
 constexpr int kTkWarps = kTkThreads / 32;
-constexpr int kPer = 4;                      // consecutive elements per thread
-constexpr int kTile = kTkThreads * kPer;     // elements per block-wide step
-constexpr int kListCap = 12288;
+constexpr int kPer = 4;                   // consecutive positions per lane per step
+constexpr int kWarpStep = 32 * kPer;      // positions per warp per step
+constexpr int kTile = kTkThreads * kPer;  // positions per block-wide step (fallback)
+constexpr int kWarpCap = 512;             // list entries per warp
+constexpr int kListCap = kWarpCap * kTkWarps;
 
 struct TkSmem {
   uint32_t hist[2048];
-  uint32_t wt[kTkWarps];
+  uint32_t wt[32];
   uint32_t res[2];
+  uint32_t wcnt[kTkWarps];  // list entries per warp
+  uint32_t wgt[kTkWarps];   // per warp: entries > T, then their exclusive prefix
+  uint32_t weq[kTkWarps];   // per warp: entries == T, then their exclusive prefix
+  uint32_t overflow;
   float lse[8];
   uint32_t keys[kListCap];
   int32_t idxs[kListCap];
@@ -51,6 +61,16 @@ __device__ __forceinline__ float key2f(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+__device__ __forceinline__ uint32_t warp_excl_scan(uint32_t v, int lane) {
+  uint32_t x = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xffffffffu, x, off);
+    if (lane >= off) x += y;
+  }
+  return x - v;
+}
+
 // Exclusive prefix sum of v over the block in thread order; *total = sum.
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wt, uint32_t* total) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -63,13 +83,13 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wt, ui
   if (lane == 31) wt[warp] = x;
   __syncthreads();
   if (warp == 0) {
-    uint32_t t = wt[lane];
+    uint32_t t = lane < kTkWarps ? wt[lane] : 0u;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
       const uint32_t y = __shfl_up_sync(0xffffffffu, t, off);
       if (lane >= off) t += y;
     }
-    wt[lane] = t;
+    if (lane < kTkWarps) wt[lane] = t;
   }
   __syncthreads();
   const uint32_t r = (warp ? wt[warp - 1] : 0u) + x - v;
@@ -83,7 +103,7 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t* wt, ui
 // and store (b, above(b)) in res.  Requires 1 <= k_rem <= sum(hist).
 __device__ void find_bin(const uint32_t* hist, int nbins, uint32_t k_rem, uint32_t* wt,
                          uint32_t* res) {
-  const int per = nbins / kTkThreads;  // 1 or 2 bins per thread, top bins first
+  const int per = nbins / kTkThreads;  // bins per thread, top bins first
   const int top = nbins - 1 - (int)threadIdx.x * per;
   uint32_t local = 0;
   for (int p = 0; p < per; ++p) local += hist[top - p];
@@ -104,7 +124,7 @@ __device__ void find_bin(const uint32_t* hist, int nbins, uint32_t k_rem, uint32
   __syncthreads();
 }
 
-// Keys of one unit read from the fp32 logits in global memory.
+// Keys of one unit computed from the fp32 logits in global memory.
 template <int G>
 struct GlobalKeys {
   const float* lg;  // logits row of the group's first query head
@@ -112,7 +132,7 @@ struct GlobalKeys {
   float lse[G];
   // Keys of positions j0..j0+3 (j0 % 4 == 0, j0 < span); entries >= span
   // hold unspecified values and must be masked by the caller.
-  __device__ __forceinline__ void load4(int j0, uint32_t (&key)[kPer], int32_t (&id)[kPer]) const {
+  __device__ __forceinline__ void load4(int j0, uint32_t (&key)[kPer]) const {
     if (G == 1) {
       const float4 v = *reinterpret_cast<const float4*>(lg + j0);
       key[0] = f2key(v.x);
@@ -132,72 +152,117 @@ struct GlobalKeys {
 #pragma unroll
       for (int e = 0; e < 4; ++e) key[e] = f2key(a[e]);
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) id[e] = j0 + e;
-  }
-  __device__ __forceinline__ int count() const { return span; }
-  __device__ __forceinline__ void get4(int e0, uint32_t (&key)[kPer], int32_t (&id)[kPer]) const {
-    if (e0 < span) load4(e0, key, id);
   }
 };
 
-// Keys compacted into the shared-memory list.
-struct ListKeys {
-  const uint32_t* keys;
-  const int32_t* idxs;
-  int n;
-  __device__ __forceinline__ int count() const { return n; }
-  __device__ __forceinline__ void get4(int e0, uint32_t (&key)[kPer], int32_t (&id)[kPer]) const {
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      if (e0 + e < n) {
-        key[e] = keys[e0 + e];
-        id[e] = idxs[e0 + e];
-      }
-    }
-  }
-};
-
-// Histogram of bits [lo, lo + nbits) of the keys whose bits above lo + nbits
-// equal `prefix` (all keys when nbits covers the top bits).
-template <class Src>
-__device__ void histogram(const Src& src, TkSmem& sm, int lo, int nbits, uint32_t prefix,
-                          bool filter) {
+// Histogram over the whole unit (block-strided) of bits [lo, lo+nbits) of the
+// keys whose higher bits equal `prefix`.
+template <int G>
+__device__ void histogram_global(const GlobalKeys<G>& src, TkSmem& sm, int lo, int nbits,
+                                 uint32_t prefix) {
   const int nb = 1 << nbits;
   for (int i = threadIdx.x; i < nb; i += kTkThreads) sm.hist[i] = 0;
   __syncthreads();
-  const int cnt = src.count();
-  for (int e0 = (int)threadIdx.x * kPer; e0 < cnt; e0 += kTile) {
+  for (int j0 = (int)threadIdx.x * kPer; j0 < src.span; j0 += kTile) {
     uint32_t key[kPer];
-    int32_t id[kPer];
-    src.get4(e0, key, id);
+    src.load4(j0, key);
 #pragma unroll
-    for (int e = 0; e < kPer; ++e) {
-      if (e0 + e < cnt) {
-        const bool take = !filter || (key[e] >> (lo + nbits)) == prefix;
-        if (take) atomicAdd(&sm.hist[(key[e] >> lo) & (uint32_t)(nb - 1)], 1u);
-      }
-    }
+    for (int e = 0; e < kPer; ++e)
+      if (j0 + e < src.span && (key[e] >> (lo + nbits)) == prefix)
+        atomicAdd(&sm.hist[(key[e] >> lo) & (uint32_t)(nb - 1)], 1u);
   }
   __syncthreads();
 }
 
-// Ordered emit: every key > T, then the first k_rem keys == T by position.
-template <class Src>
-__device__ void emit(const Src& src, TkSmem& sm, uint32_t T, uint32_t k_rem, int k,
-                     int32_t* idx_out, float* sel_out, bool mha, float lse0) {
-  const int cnt = src.count();
+// Histogram over the per-warp lists (each warp walks its own list).
+__device__ void histogram_lists(TkSmem& sm, int lo, int nbits, uint32_t prefix) {
+  const int nb = 1 << nbits;
+  for (int i = threadIdx.x; i < nb; i += kTkThreads) sm.hist[i] = 0;
+  __syncthreads();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t* keys = sm.keys + warp * kWarpCap;
+  const int cnt = (int)sm.wcnt[warp];
+  for (int e = lane; e < cnt; e += 32) {
+    const uint32_t key = keys[e];
+    if ((key >> (lo + nbits)) == prefix) atomicAdd(&sm.hist[(key >> lo) & (uint32_t)(nb - 1)], 1u);
+  }
+  __syncthreads();
+}
+
+// Score written for a selected key: alpha (MHA) or the group score itself.
+__device__ __forceinline__ float sel_value(uint32_t key, bool mha, float lse0) {
+  const float v = key2f(key);
+  return mha ? expf(v - lse0) : v;
+}
+
+// Ordered emit over the per-warp lists: every key > T, then the first k_rem
+// keys == T in position order.
+__device__ void emit_lists(TkSmem& sm, uint32_t T, uint32_t k_rem, int k, int32_t* idx_out,
+                           float* sel_out, bool mha, float lse0) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint32_t* keys = sm.keys + warp * kWarpCap;
+  const int32_t* idxs = sm.idxs + warp * kWarpCap;
+  const int cnt = (int)sm.wcnt[warp];
+  uint32_t ngt = 0, neq = 0;
+  for (int e = lane; e < cnt; e += 32) {
+    ngt += keys[e] > T;
+    neq += keys[e] == T;
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    ngt += __shfl_xor_sync(0xffffffffu, ngt, off);
+    neq += __shfl_xor_sync(0xffffffffu, neq, off);
+  }
+  if (lane == 0) {
+    sm.wgt[warp] = ngt;
+    sm.weq[warp] = neq;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t g = lane < kTkWarps ? sm.wgt[lane] : 0u;
+    const uint32_t q = lane < kTkWarps ? sm.weq[lane] : 0u;
+    const uint32_t gx = warp_excl_scan(g, lane), qx = warp_excl_scan(q, lane);
+    if (lane < kTkWarps) {
+      sm.wgt[lane] = gx;
+      sm.weq[lane] = qx;
+    }
+  }
+  __syncthreads();
+  uint32_t gb = sm.wgt[warp], eb = sm.weq[warp];  // counts before this warp's segment
+  const unsigned lt_mask = (1u << lane) - 1u;
+  for (int e0 = 0; e0 < cnt; e0 += 32) {
+    const int e = e0 + lane;
+    const bool v = e < cnt;
+    const uint32_t key = v ? keys[e] : 0u;
+    const bool gt = v && key > T, eq = v && key == T;
+    const unsigned bg = __ballot_sync(0xffffffffu, gt), bq = __ballot_sync(0xffffffffu, eq);
+    const uint32_t g_before = gb + __popc(bg & lt_mask), q_before = eb + __popc(bq & lt_mask);
+    int pos = -1;
+    if (gt) pos = (int)(g_before + min(q_before, k_rem));
+    else if (eq && q_before < k_rem) pos = (int)(g_before + q_before);
+    if (pos >= 0 && pos < k) {
+      idx_out[pos] = idxs[e];
+      sel_out[pos] = sel_value(key, mha, lse0);
+    }
+    gb += __popc(bg);
+    eb += __popc(bq);
+  }
+}
+
+// Ordered emit over global memory (fallback), block-wide in tiles.
+template <int G>
+__device__ void emit_global(const GlobalKeys<G>& src, TkSmem& sm, uint32_t T, uint32_t k_rem,
+                            int k, int32_t* idx_out, float* sel_out, bool mha, float lse0) {
   uint32_t cgt = 0, ceq = 0;
-  for (int t0 = 0; t0 < cnt; t0 += kTile) {
-    const int e0 = t0 + (int)threadIdx.x * kPer;
+  for (int t0 = 0; t0 < src.span; t0 += kTile) {
+    const int j0 = t0 + (int)threadIdx.x * kPer;
     uint32_t key[kPer] = {0u, 0u, 0u, 0u};
-    int32_t id[kPer] = {0, 0, 0, 0};
-    src.get4(e0, key, id);
+    if (j0 < src.span) src.load4(j0, key);
     bool gt[kPer], eq[kPer];
     uint32_t ngt = 0, neq = 0;
 #pragma unroll
     for (int e = 0; e < kPer; ++e) {
-      const bool v = e0 + e < cnt;
+      const bool v = j0 + e < src.span;
       gt[e] = v && key[e] > T;
       eq[e] = v && key[e] == T;
       ngt += gt[e];
@@ -217,9 +282,8 @@ __device__ void emit(const Src& src, TkSmem& sm, uint32_t T, uint32_t k_rem, int
         ++eb;
       }
       if (pos >= 0 && pos < k) {
-        const float v = key2f(key[e]);
-        idx_out[pos] = id[e];
-        sel_out[pos] = mha ? expf(v - lse0) : v;
+        idx_out[pos] = j0 + e;
+        sel_out[pos] = sel_value(key[e], mha, lse0);
       }
     }
     cgt += tot & 0xFFFFu;
@@ -228,7 +292,7 @@ __device__ void emit(const Src& src, TkSmem& sm, uint32_t T, uint32_t k_rem, int
 }
 
 template <int G>
-__global__ void __launch_bounds__(kTkThreads, 1)
+__global__ void __launch_bounds__(kTkThreads)
     topk_kernel(const float* __restrict__ logits, const float2* __restrict__ part,
                 int32_t* __restrict__ idx_out, float* __restrict__ sel_out,
                 float* __restrict__ lse_out, int Hq, int Hkv, int ldn, int span, int k,
@@ -256,6 +320,8 @@ __global__ void __launch_bounds__(kTkThreads, 1)
       if (lse_out) lse_out[b * Hq + hk * G + warp] = lse;
     }
   }
+  if (threadIdx.x == 0) sm.overflow = 0;
+  for (int i = threadIdx.x; i < 2048; i += kTkThreads) sm.hist[i] = 0;
   __syncthreads();
 
   GlobalKeys<G> src;
@@ -267,70 +333,93 @@ __global__ void __launch_bounds__(kTkThreads, 1)
   int32_t* idx_u = idx_out + (size_t)u * k;
   float* sel_u = sel_out + (size_t)u * k;
 
+  // This warp's segment of positions: [seg0, seg1), seg0 a multiple of 4.
+  const int per_warp =
+      ((span + kTkWarps - 1) / kTkWarps + kWarpStep - 1) / kWarpStep * kWarpStep;
+  const int seg0 = min(span, warp * per_warp), seg1 = min(span, seg0 + per_warp);
+
   // Pass A: bucket of the k-th largest key by its top 11 bits.
-  histogram(src, sm, 21, 11, 0u, false);
+  for (int j0 = seg0 + lane * kPer; j0 < seg1; j0 += kWarpStep) {
+    uint32_t key[kPer];
+    src.load4(j0, key);
+#pragma unroll
+    for (int e = 0; e < kPer; ++e)
+      if (j0 + e < seg1) atomicAdd(&sm.hist[key[e] >> 21], 1u);
+  }
+  __syncthreads();
   find_bin(sm.hist, 2048, (uint32_t)k, sm.wt, sm.res);
   const uint32_t b1 = sm.res[0];
-  const uint32_t above1 = sm.res[1];
-  const uint32_t in_b1 = sm.hist[b1];
-  uint32_t k_rem = (uint32_t)k - above1;
+  uint32_t k_rem = (uint32_t)k - sm.res[1];
   __syncthreads();
 
-  if (above1 + in_b1 <= (uint32_t)kListCap) {
-    // Pass B: ordered compaction of every key in buckets >= b1.
-    uint32_t nlist = 0;
-    for (int t0 = 0; t0 < span; t0 += kTile) {
-      const int j0 = t0 + (int)threadIdx.x * kPer;
+  // Pass B: each warp compacts its keys in buckets >= b1, in position order.
+  {
+    uint32_t* keys = sm.keys + warp * kWarpCap;
+    int32_t* idxs = sm.idxs + warp * kWarpCap;
+    uint32_t n_w = 0;
+    bool over = false;
+    for (int base = seg0; base < seg1; base += kWarpStep) {
+      const int j0 = base + lane * kPer;
       uint32_t key[kPer] = {0u, 0u, 0u, 0u};
-      int32_t id[kPer];
-      if (j0 < span) src.load4(j0, key, id);
+      if (j0 < seg1) src.load4(j0, key);
       bool f[kPer];
       uint32_t c = 0;
 #pragma unroll
       for (int e = 0; e < kPer; ++e) {
-        f[e] = (j0 + e < span) && (key[e] >> 21) >= b1;
+        f[e] = (j0 + e < seg1) && (key[e] >> 21) >= b1;
         c += f[e];
       }
-      uint32_t tot;
-      uint32_t pos = nlist + block_excl_scan(c, sm.wt, &tot);
+      uint32_t pos = n_w + warp_excl_scan(c, lane);
+      uint32_t tot = c;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+      if (n_w + tot > (uint32_t)kWarpCap) {
+        over = true;  // the same decision in every lane
+        break;
+      }
 #pragma unroll
       for (int e = 0; e < kPer; ++e) {
         if (f[e]) {
-          sm.keys[pos] = key[e];
-          sm.idxs[pos] = j0 + e;
+          keys[pos] = key[e];
+          idxs[pos] = j0 + e;
           ++pos;
         }
       }
-      nlist += tot;
+      n_w += tot;
     }
-    __syncthreads();
-    ListKeys list{sm.keys, sm.idxs, (int)nlist};
-    histogram(list, sm, 10, 11, b1, true);
+    if (lane == 0) {
+      sm.wcnt[warp] = n_w;
+      if (over) atomicOr(&sm.overflow, 1u);
+    }
+  }
+  __syncthreads();
+
+  uint32_t T;
+  if (!sm.overflow) {
+    histogram_lists(sm, 10, 11, b1);
     find_bin(sm.hist, 2048, k_rem, sm.wt, sm.res);
-    const uint32_t b2 = sm.res[0];
+    const uint32_t pre = (b1 << 11) | sm.res[0];
     k_rem -= sm.res[1];
     __syncthreads();
-    const uint32_t pre = (b1 << 11) | b2;
-    histogram(list, sm, 0, 10, pre, true);
+    histogram_lists(sm, 0, 10, pre);
     find_bin(sm.hist, 1024, k_rem, sm.wt, sm.res);
-    const uint32_t T = (pre << 10) | sm.res[0];
+    T = (pre << 10) | sm.res[0];
     k_rem -= sm.res[1];
     __syncthreads();
-    emit(list, sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
+    emit_lists(sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
   } else {
-    // Overflow: resolve the remaining bits and emit from global memory.
-    histogram(src, sm, 10, 11, b1, true);
+    // A warp list overflowed: resolve the remaining bits and emit from global memory.
+    histogram_global(src, sm, 10, 11, b1);
     find_bin(sm.hist, 2048, k_rem, sm.wt, sm.res);
-    const uint32_t b2 = sm.res[0];
+    const uint32_t pre = (b1 << 11) | sm.res[0];
     k_rem -= sm.res[1];
     __syncthreads();
-    const uint32_t pre = (b1 << 11) | b2;
-    histogram(src, sm, 0, 10, pre, true);
+    histogram_global(src, sm, 0, 10, pre);
     find_bin(sm.hist, 1024, k_rem, sm.wt, sm.res);
-    const uint32_t T = (pre << 10) | sm.res[0];
+    T = (pre << 10) | sm.res[0];
     k_rem -= sm.res[1];
     __syncthreads();
-    emit(src, sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
+    emit_global(src, sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
   }
 }
 
@@ -340,8 +429,8 @@ cudaError_t launch_typed(const Dims& d, const float* logits, const float2* part,
   static unsigned long long prepared = 0;
   cudaError_t e = prepare_kernel(topk_kernel<G>, &prepared, (int)sizeof(TkSmem));
   if (e != cudaSuccess) return e;
-  topk_kernel<G><<<d.U, kTkThreads, sizeof(TkSmem), st>>>(logits, part, idx, sel, lse, d.Hq, d.Hkv,
-                                                          d.ldn, d.span, d.k, d.nchunks);
+  topk_kernel<G><<<d.U, kTkThreads, sizeof(TkSmem), st>>>(logits, part, idx, sel, lse, d.Hq,
+                                                          d.Hkv, d.ldn, d.span, d.k, d.nchunks);
   return cudaGetLastError();
 }
 

@@ -33,15 +33,19 @@ def orc_shape(w) -> oracle.Shape:
 class Slot:
     """One layer slot: pinned host store (q_spec, q, K, V) and device copies."""
 
-    def __init__(self, w, slot: int = 0, device: str = "cuda", fill=True):
+    def __init__(self, w, slot: int = 0, device: str = "cuda", fill=True, huge_pages=False):
         dt = torch_dtype(w)
         B, Hq, Hkv, d, n, W = (w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.ctx_len,
                                w.window)
         self.w = w
         self.q_spec_h = torch.empty((B, Hq, d), dtype=dt, pin_memory=True)
         self.q_h = torch.empty((B, Hq, d), dtype=dt, pin_memory=True)
-        self.K_h = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
-        self.V_h = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
+        if huge_pages:  # the library's host store allocator
+            self.K_h = dd.host_empty((B, Hkv, n, d), dt)
+            self.V_h = dd.host_empty((B, Hkv, n, d), dt)
+        else:  # plain page-locked memory from torch
+            self.K_h = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
+            self.V_h = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
         self.planted = np.zeros((B, Hkv, max(w.n_planted, 1)), np.int32)
         if fill:
             synth.fill_slot(w, slot, self.q_spec_h, self.q_h, self.K_h, self.V_h, self.planted)
