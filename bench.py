@@ -55,6 +55,14 @@ def parse():
                    help="0: bulk-copy gather, 1: load/store gather")
     p.add_argument("--host-alloc", default="pinned", choices=["huge", "pinned"],
                    help="host KV store: dd_host_alloc huge pages, or torch pinned memory")
+    p.add_argument("--copy-priority", default="high", choices=["high", "low"],
+                   help="priority of the copy stream relative to the compute stream")
+    p.add_argument("--slots", type=int, default=0,
+                   help="override the number of distinct layer slots (memory-limited runs)")
+    p.add_argument("--schedule", default="overlap", choices=["overlap", "late", "pipeline"],
+                   help="overlap: gather l+1 beside attention l; late: gather l+1 after "
+                        "attention l; pipeline: gather and attention of each layer on the "
+                        "copy stream")
     p.add_argument("--late-gather", type=int, default=0,
                    help="1: start each layer's gather after the previous attention")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -66,6 +74,8 @@ def workload(args):
     w = synth.WORKLOADS[args.workload]
     if args.profile_case:
         w = w.scaled(batch=2, n_layers=2, n_slots=1)
+    if args.slots:
+        w = w.scaled(n_slots=args.slots)
     return w
 
 
@@ -209,7 +219,8 @@ def config_of(w, args):
                   % (w.k_bytes() / 2**20),
             "parallelism": f"replicas x{args.gpus} (independent requests per GPU)",
             "gather_mode": ["bulk_copy", "load_store"][args.gather_mode],
-            "host_store": args.host_alloc, "late_gather": bool(args.late_gather)}
+            "host_store": args.host_alloc, "schedule": args.schedule,
+            "copy_stream_priority": args.copy_priority}
 
 
 def run_reference(args, rank, world):
@@ -273,8 +284,12 @@ def run_ours(args, rank, world):
 
     shape = dd.Shape(B, Hq, Hkv, d, n, k, W, w.dtype)
     ctx = dd.Ctx(shape)
-    compute = torch.cuda.Stream()
-    copy = torch.cuda.Stream(priority=-1)
+    late = bool(args.late_gather) or args.schedule == "late"
+    pipe = args.schedule == "pipeline"
+    if args.copy_priority == "high":
+        compute, copy = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    else:
+        compute, copy = torch.cuda.Stream(priority=-1), torch.cuda.Stream()
     layers = dd.Ctx.pack([dd.LayerIO(qs_d[l % D], q_d[l % D], K_d[l % D], K_h[l % D],
                                      V_h[l % D], vwin_d[l % D] if W > 0 else None, outs[l])
                           for l in range(L)])
@@ -324,7 +339,7 @@ def run_ours(args, rank, world):
 
     def step(copy_stream, timing=True):
         ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
-                        late_gather=args.late_gather, gather_mode=args.gather_mode)
+                        late_gather=late, pipeline=pipe, gather_mode=args.gather_mode)
         return ctx.timings() if timing else None
 
     compute.wait_stream(torch.cuda.current_stream())
@@ -373,7 +388,7 @@ def run_ours(args, rank, world):
         with torch.cuda.stream(compute):
             qs_l.copy_(qs_src, non_blocking=True)
             q_l.copy_(q_src, non_blocking=True)
-        ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=args.late_gather,
+        ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=late, pipeline=pipe,
                         gather_mode=args.gather_mode)
         with torch.cuda.stream(compute):
             out_h.copy_(outs, non_blocking=True)

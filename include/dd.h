@@ -254,8 +254,13 @@ enum {
   DD_STEP_TIMING = 1,     /* record per-phase CUDA events; read with dd_ctx_timings */
   DD_STEP_LATE_GATHER = 2, /* start the gather of layer l+1 after the attention of
                               layer l (it then overlaps the scoring of layer l+2) */
-  DD_STEP_GATHER_LSU = 4   /* gather with dd_gather_h2d mode 1 (load/store)
+  DD_STEP_GATHER_LSU = 4,  /* gather with dd_gather_h2d mode 1 (load/store)
                               instead of mode 0 (bulk copy) */
+  DD_STEP_PIPELINE = 8     /* two-stage pipeline: scoring and top-k of every
+                              layer on `compute`; the gather and then the
+                              attention of each layer on `copy`, as soon as its
+                              indices are ready (compute runs at most two layers
+                              ahead); attention never runs beside a gather */
 };
 
 /*

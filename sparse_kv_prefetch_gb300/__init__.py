@@ -25,6 +25,7 @@ DD_F32, DD_BF16 = 0, 1
 DD_STEP_TIMING = 1
 DD_STEP_LATE_GATHER = 2
 DD_STEP_GATHER_LSU = 4
+DD_STEP_PIPELINE = 8
 
 
 class DDError(RuntimeError):
@@ -273,13 +274,14 @@ class Ctx:
         return arr
 
     def decode_step(self, layers, compute=None, copy=None, timing: bool = False,
-                    late_gather: bool = False, gather_mode: int = 0):
+                    late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
         flags = ((DD_STEP_TIMING if timing else 0) | (DD_STEP_LATE_GATHER if late_gather else 0)
-                 | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0))
+                 | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
+                 | (DD_STEP_PIPELINE if pipeline else 0))
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 

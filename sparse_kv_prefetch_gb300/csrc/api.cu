@@ -510,20 +510,24 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     return cudaEventRecord(c->ev_ready[s], X);
   };
   // Step 4 of layer l from scratch slot l % 2 (on the compute stream).
+  // In the pipeline schedule the attention runs on the copy stream, right
+  // after the gather of the same layer; otherwise on the compute stream.
+  const bool pipeline = !serial && (flags & DD_STEP_PIPELINE) != 0;
+  cudaStream_t A = pipeline ? X : C;
   auto attend = [&](int l) -> cudaError_t {
     const int s = l & 1;
     cudaError_t e;
-    if (!serial) {
+    if (!serial && !pipeline) {
       e = cudaStreamWaitEvent(C, c->ev_ready[s], 0);
       if (e != cudaSuccess) return e;
     }
-    if (timing) cudaEventRecord(T(l, PH_ATTN0), C);
+    if (timing) cudaEventRecord(T(l, PH_ATTN0), A);
     e = launch_attn(d, layers[l].q, c->kbuf[s], c->vbuf[s], layers[l].k_dev, layers[l].v_win,
-                    layers[l].out, attn_o, attn_ml, C);
+                    layers[l].out, attn_o, attn_ml, A);
     if (e != cudaSuccess) return e;
-    if (timing) cudaEventRecord(T(l, PH_ATTN1), C);
+    if (timing) cudaEventRecord(T(l, PH_ATTN1), A);
     launches += kAttnLaunches;
-    return cudaEventRecord(c->ev_free[s], C);
+    return cudaEventRecord(c->ev_free[s], A);
   };
 
   if (timing) DD_TRY(cudaEventRecord(c->t_begin, C));
@@ -533,6 +537,21 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       DD_TRY(gather(l));
       DD_TRY(attend(l));
     }
+  } else if (pipeline) {
+    // Two-stage pipeline: compute scores and selects layer after layer; the
+    // copy stream gathers and attends each layer as soon as its indices are
+    // ready.  Before topk(l) reuses index slot l % 2 (and gather(l) the
+    // scratch slot), compute waits for attention(l - 2), the last reader.
+    DD_TRY(cudaEventRecord(c->ev_join, C));
+    DD_TRY(cudaStreamWaitEvent(X, c->ev_join, 0));
+    for (int l = 0; l < n_layers; ++l) {
+      if (l >= 2) DD_TRY(cudaStreamWaitEvent(C, c->ev_free[l & 1], 0));
+      DD_TRY(score_topk(l));
+      DD_TRY(gather(l));
+      DD_TRY(attend(l));
+    }
+    DD_TRY(cudaEventRecord(c->ev_join, X));
+    DD_TRY(cudaStreamWaitEvent(C, c->ev_join, 0));
   } else {
     // The copy stream starts after everything already queued on compute
     // (the previous step may still be reading a scratch slot).

@@ -86,6 +86,9 @@ unsigned int take_gather_status();
 
 // ----------------------------------------------------------------- device
 
+// log2 of a power of two, at compile time.
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
 // Rows of K / V are moved as 16-byte vectors: 8 bf16 or 4 fp32 elements.
 template <typename T>
 struct Elem;

@@ -55,6 +55,10 @@ __global__ void __launch_bounds__(kScoreThreads)
   using Geo = ScoreGeom<T, D>;
   constexpr int VEC = Geo::kVec, LPR = Geo::kLpr, RPW = Geo::kRpw, NG = Geo::kGroups;
   constexpr int SR = Geo::kStageRows, RPG = Geo::kRowsPerGroup, RB = Geo::kRowBytes;
+  constexpr int N = G * RPG;                     // partial sums per lane per stage
+  constexpr int S = ilog2(N) < ilog2(LPR) ? ilog2(N) : ilog2(LPR);  // transposing steps
+  constexpr int P = N >> S;                      // totals per lane after the reduction
+  static_assert(P <= RPG && RPG % P == 0, "a lane's totals must share one head");
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
@@ -78,12 +82,9 @@ __global__ void __launch_bounds__(kScoreThreads)
   }
   __syncthreads();
 
-  float m_run[G], l_run[G];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m_run[g] = -INFINITY;
-    l_run[g] = 0.f;
-  }
+  // Running (max, sum of exp) of the logits this lane writes (one head).
+  float m_run = -INFINITY, l_run = 0.f;
+  int head = -1;  // the lane's head; -1 for lanes that write nothing
   bool ok = true;
   const unsigned char* Ku = K + (size_t)u * n * RB;
 
@@ -111,6 +112,19 @@ __global__ void __launch_bounds__(kScoreThreads)
     for (int g = 0; g < G; ++g)
       unpack(ld_ro(q_spec + ((size_t)(b * Hq + hk * G + g)) * LPR + sub), qf[g]);
 
+    // After the transposed reduction below, lane `sub` holds the totals of
+    // the P values with indices prefix*P + p (p < P), index = g*RPG + i for
+    // head g and stage row i; prefix is `sub`'s low S bits reversed.  Only
+    // lanes with sub < 2^S hold distinct values, and all of one lane's values
+    // belong to the same head g_lane.
+    int prefix = 0;
+#pragma unroll
+    for (int t = 0; t < S; ++t) prefix |= ((sub >> t) & 1) << (S - 1 - t);
+    const int g_lane = (prefix * P) / RPG;
+    const bool writer = (sub >> S) == 0;
+    if (writer) head = g_lane;
+    float* lg_row = logits + (size_t)(b * Hq + hk * G + g_lane) * ldn;
+
     for (int t = 0; t < n_stages; ++t) {
       const int s = t % kStages;
       if (!mbar_wait(&full[s], (t / kStages) & 1)) {
@@ -120,7 +134,7 @@ __global__ void __launch_bounds__(kScoreThreads)
       const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * kStageBytes);
       const int r0 = j_begin + t * SR;
       // Row (i * NG + grp) of the stage, for i < RPG, belongs to this lane group.
-      float acc[G][RPG];
+      float acc[N];
 #pragma unroll
       for (int i = 0; i < RPG; ++i) {
         float kf[VEC];
@@ -130,31 +144,42 @@ __global__ void __launch_bounds__(kScoreThreads)
           float a = 0.f;
 #pragma unroll
           for (int e = 0; e < VEC; ++e) a = fmaf(qf[g][e], kf[e], a);
-          acc[g][i] = a;
+          acc[g * RPG + i] = a;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+      // Transposed reduction over the LPR lanes of the group: at step t each
+      // lane keeps one half of its values, sends the other half to the lane
+      // 2^t away and adds what it receives, so the number of values halves.
 #pragma unroll
-      for (int off = LPR / 2; off > 0; off >>= 1)
+      for (int t2 = 0; t2 < S; ++t2) {
+        const int half = (N >> t2) / 2;
+        const bool up = (sub >> t2) & 1;
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int i = 0; i < half; ++i) {
+          const float send = up ? acc[i] : acc[i + half];
+          const float keep = up ? acc[i + half] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << t2);
+        }
+      }
+      // Remaining lane bits: plain butterfly on the P values left.
 #pragma unroll
-          for (int i = 0; i < RPG; ++i) acc[g][i] += __shfl_xor_sync(0xffffffffu, acc[g][i], off);
-      // Lane `sub` of the group owns row i == sub.
-      const int j = r0 + sub * NG + grp;
-      if (sub < RPG && j < j_end) {
+      for (int off = 1 << S; off < LPR; off <<= 1)
 #pragma unroll
-        for (int g = 0; g < G; ++g) {
-          float sv = 0.f;
+        for (int p = 0; p < P; ++p) acc[p] += __shfl_xor_sync(0xffffffffu, acc[p], off);
+      if (writer) {
 #pragma unroll
-          for (int i = 0; i < RPG; ++i)
-            if (i == sub) sv = acc[g][i];
-          sv *= scale;
-          logits[(size_t)(b * Hq + hk * G + g) * ldn + j] = sv;
-          const float m_new = fmaxf(m_run[g], sv);
-          l_run[g] = l_run[g] * __expf(m_run[g] - m_new) + __expf(sv - m_new);
-          m_run[g] = m_new;
+        for (int p = 0; p < P; ++p) {
+          const int i = (prefix * P + p) % RPG;
+          const int j = r0 + i * NG + grp;
+          if (j < j_end) {
+            const float sv = acc[p] * scale;
+            lg_row[j] = sv;
+            const float m_new = fmaxf(m_run, sv);
+            l_run = l_run * __expf(m_run - m_new) + __expf(sv - m_new);
+            m_run = m_new;
+          }
         }
       }
     }
@@ -173,7 +198,7 @@ __global__ void __launch_bounds__(kScoreThreads)
   __shared__ float2 red[G][kConsumerWarps + 1];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    float2 p = make_float2(m_run[g], l_run[g]);
+    float2 p = head == g ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       float2 o;

@@ -180,10 +180,13 @@ def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
     ctx.decode_step(_layers(w, slots, outs_b, L), compute=compute, copy=None)
     outs_c = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
     ctx.decode_step(_layers(w, slots, outs_c, L), compute=compute, copy=copy, late_gather=True)
+    outs_d = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
+    ctx.decode_step(_layers(w, slots, outs_d, L), compute=compute, copy=copy, pipeline=True)
     torch.cuda.synchronize()
     for l in range(L):
         assert torch.equal(outs_a[l], outs_b[l]), f"layer {l}: overlapped != serial"
         assert torch.equal(outs_c[l], outs_b[l]), f"layer {l}: late gather != serial"
+        assert torch.equal(outs_d[l], outs_b[l]), f"layer {l}: pipeline != serial"
         assert torch.equal(outs_a[l], ref[l % D]), f"layer {l}: step != per-layer calls"
     assert t["n_layers"] == L and t["launches"] == L * 6
     assert t["step_ms"] > 0 and t["score_ms"] > 0 and t["gather_ms"] > 0
