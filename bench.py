@@ -36,10 +36,10 @@ METRIC = "sparse-decode layer-steps/s; scoring HBM GB/s; gather host-link GB/s"
 UNIT = "layer-steps/s"
 FALLBACK_HBM_GBS = 6800.0
 # DRAM read + write bytes of one score_kernel launch, from the ncu capture in
-# profiles/score_kernel_7b32k-batch2.md (batch 2: 546.75 MB for 64 units),
+# profiles/score_kernel_7b32k-batch2.md (batch 2: 546.77 MB for 64 units),
 # scaled by units to the 7B-32K layer (256 units); traffic grows with the
 # units processed.  Keyed by workload; None where no capture exists.
-SCORE_TRAFFIC_BYTES = {"c2-7b-32k": 546.75e6 * 256 / 64}
+SCORE_TRAFFIC_BYTES = {"c2-7b-32k": 546.77e6 * 256 / 64}
 
 
 def parse():
@@ -63,6 +63,8 @@ def parse():
                    help="overlap: gather l+1 beside attention l; late: gather l+1 after "
                         "attention l; pipeline: gather and attention of each layer on the "
                         "copy stream")
+    p.add_argument("--correct-misses", action="store_true",
+                   help="correct prediction misses in every timed layer (DD_STEP_CORRECT_MISSES)")
     p.add_argument("--late-gather", type=int, default=0,
                    help="1: start each layer's gather after the previous attention")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -220,7 +222,8 @@ def config_of(w, args):
             "parallelism": f"replicas x{args.gpus} (independent requests per GPU)",
             "gather_mode": ["bulk_copy", "load_store"][args.gather_mode],
             "host_store": args.host_alloc, "schedule": args.schedule,
-            "copy_stream_priority": args.copy_priority}
+            "copy_stream_priority": args.copy_priority,
+            "correct_misses": bool(args.correct_misses)}
 
 
 def run_reference(args, rank, world):
@@ -335,11 +338,39 @@ def run_ours(args, rank, world):
         e1.record(compute)
         e1.synchronize()
         gather_alone[mode] = w.gather_bytes() * 4 * D / (e0.elapsed_time(e1) * 1e-3) / 1e9
+
+    # Predictability: for every layer slot, the rows prefetched with q_spec
+    # against the real query's own top-k (dd_correct_misses).
+    pred_miss, pred_mass = [], []
+    if k <= 4096:
+        c_idx = torch.empty((U, k), dtype=torch.int32, device=dev)
+        c_kb, c_vb = torch.empty_like(g_kb), torch.empty_like(g_vb)
+        c_miss = torch.empty(U, dtype=torch.int32, device=dev)
+        c_mass = torch.empty((U, 2), dtype=torch.float32, device=dev)
+        for s_ in range(D):
+            dd.gather_h2d(shape, K_h[s_], V_h[s_], g_idx[s_], g_kb, g_vb, stream=compute)
+            dd.correct_misses(shape, q_d[s_], K_d[s_], g_idx[s_], g_kb, g_vb, K_h[s_], V_h[s_],
+                              c_idx, c_kb, c_vb, c_miss, c_mass, g_ws, stream=compute)
+            compute.synchronize()
+            pred_miss.append(c_miss.cpu().numpy().copy())
+            pred_mass.append(c_mass.cpu().numpy().copy())
+        del c_kb, c_vb
+    predictability = None
+    if pred_miss:
+        pm, ms = np.stack(pred_miss), np.stack(pred_mass)
+        predictability = {
+            "recall": float(1.0 - pm.mean() / k),
+            "recall_min_unit": float(1.0 - pm.max() / k),
+            "mass_recall": float(ms[..., 0].sum() / ms[..., 1].sum()),
+            "what": "|TopK(q_spec) & TopK(q)| / k and the real query's selection score "
+                    "captured by the prefetched rows, over all layer slots and units",
+        }
     del g_ws, g_kb, g_vb
 
     def step(copy_stream, timing=True):
         ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
-                        late_gather=late, pipeline=pipe, gather_mode=args.gather_mode)
+                        late_gather=late, pipeline=pipe, gather_mode=args.gather_mode,
+                        correct_misses=args.correct_misses)
         return ctx.timings() if timing else None
 
     compute.wait_stream(torch.cuda.current_stream())
@@ -389,7 +420,7 @@ def run_ours(args, rank, world):
             qs_l.copy_(qs_src, non_blocking=True)
             q_l.copy_(q_src, non_blocking=True)
         ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=late, pipeline=pipe,
-                        gather_mode=args.gather_mode)
+                        gather_mode=args.gather_mode, correct_misses=args.correct_misses)
         with torch.cuda.stream(compute):
             out_h.copy_(outs, non_blocking=True)
     for _ in range(2):
@@ -467,6 +498,7 @@ def run_ours(args, rank, world):
                 "d2h_bytes_per_step": L * B * Hq * d * 4,
                 "gather_host_bytes_per_step": L * g_bytes},
         "gpu_launches": launches,
+        "predictability": predictability,
         "clocks": clk,
         "setup_s": {"generate": t_gen},
         "host_store": {"bytes": store_bytes, "huge_page_bytes": dd.host_page_bytes(),

@@ -223,6 +223,34 @@ dd_status dd_sparse_decode_attn_noalloc(const dd_shape* shape, const void* q, co
                                         const void* v_buf, const void* k_dev, const void* v_win,
                                         float* out, dd_stream_t stream);
 
+/*
+ * Miss correction for one layer, once the real query is known (paper Sec. 1:
+ * the transfer schedule corrects prediction misses on the critical path;
+ * summary page, weaknesses: a misprediction falls back to synchronous
+ * retrieval).  Computes the real query's top-k exactly as dd_score_topk does
+ * (idx_true_out, ascending), then writes its rows to k_buf_out / v_buf_out in
+ * idx_true order: a row already in the prefetched buffers (idx_spec, k_buf_spec,
+ * v_buf_spec, as left by dd_score_topk and dd_gather_h2d with the speculated
+ * query) is copied on the device, a missed row is read from the pinned host
+ * store.  miss_out[u] (optional) counts the missed rows of unit u; mass_out
+ * (optional) is [B*H_kv][2]: the real query's selection score (alpha, or its
+ * group sum) over the rows that were prefetched, and over all k rows.
+ *   q            device [B][H_q][d]      the real query
+ *   idx_spec     device [B][H_kv][k]     ascending, from the prediction
+ *   k_buf_spec, v_buf_spec device [B][H_kv][k][d]
+ *   k_host, v_host pinned host [B][H_kv][n][d]
+ *   idx_true_out device [B][H_kv][k] int32
+ *   k_buf_out, v_buf_out device [B][H_kv][k][d] (must not alias the inputs)
+ * k above 4096 returns DD_ERR_UNSUPPORTED.  Uses the workspace of
+ * dd_workspace_size.
+ */
+dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_dev,
+                            const int32_t* idx_spec, const void* k_buf_spec,
+                            const void* v_buf_spec, const void* k_host, const void* v_host,
+                            int32_t* idx_true_out, void* k_buf_out, void* v_buf_out,
+                            int32_t* miss_out, float* mass_out, void* workspace, size_t ws_bytes,
+                            dd_stream_t stream);
+
 /* ---------------------------- layer loop ---------------------------- */
 
 typedef struct dd_ctx dd_ctx;
@@ -256,6 +284,12 @@ enum {
                               layer l (it then overlaps the scoring of layer l+2) */
   DD_STEP_GATHER_LSU = 4,  /* gather with dd_gather_h2d mode 1 (load/store)
                               instead of mode 0 (bulk copy) */
+  DD_STEP_CORRECT_MISSES = 16, /* before each layer's attention, compute the
+                              real query's own top-k and attend over exactly those
+                              rows, fetching the ones the prediction missed
+                              (dd_correct_misses; k <= 4096; not combinable with
+                              DD_STEP_PIPELINE); statistics via
+                              dd_ctx_correction_stats */
   DD_STEP_PIPELINE = 8     /* two-stage pipeline: scoring and top-k of every
                               layer on `compute`; the gather and then the
                               attention of each layer on `copy`, as soon as its
@@ -289,6 +323,15 @@ typedef struct {
 
 /* Wait for the last timed step and read its phase times. */
 dd_status dd_ctx_timings(dd_ctx* ctx, dd_phase_times* out);
+
+/*
+ * Miss statistics of the last step run with DD_STEP_CORRECT_MISSES, for its
+ * first n_layers layers (waits for that step): misses [n_layers][B*H_kv]
+ * (rows of the real query's top-k that the prediction had not fetched) and
+ * mass [n_layers][B*H_kv][2] (the real query's selection score summed over the
+ * rows the prediction had fetched, and over all k rows).  Either may be NULL.
+ */
+dd_status dd_ctx_correction_stats(dd_ctx* ctx, int32_t* misses, float* mass, int n_layers);
 
 /* Per-layer scoring-kernel times (ms) of the last timed step; n entries max. */
 dd_status dd_ctx_score_times(dd_ctx* ctx, float* out_ms, int n);

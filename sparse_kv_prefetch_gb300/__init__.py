@@ -26,6 +26,7 @@ DD_STEP_TIMING = 1
 DD_STEP_LATE_GATHER = 2
 DD_STEP_GATHER_LSU = 4
 DD_STEP_PIPELINE = 8
+DD_STEP_CORRECT_MISSES = 16
 
 
 class DDError(RuntimeError):
@@ -100,6 +101,9 @@ def _lib():
             "dd_ctx_timings": ([P, ctypes.POINTER(dd_phase_times)], ctypes.c_int),
             "dd_ctx_score_times": ([P, ctypes.POINTER(ctypes.c_float), ctypes.c_int],
                                    ctypes.c_int),
+            "dd_correct_misses": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
+                                  ctypes.c_int),
+            "dd_ctx_correction_stats": ([P, P, P, ctypes.c_int], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -216,6 +220,20 @@ def sparse_decode_attn(shape: Shape, q, k_buf, v_buf, k_dev, v_win, out, workspa
            "dd_sparse_decode_attn")
 
 
+def correct_misses(shape: Shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, k_host, v_host,
+                   idx_true_out, k_buf_out, v_buf_out, miss_out, mass_out, workspace,
+                   stream=None, ws_bytes: Optional[int] = None):
+    """Miss correction for one layer: the real query's top-k and its rows,
+    copied from the prefetched buffers or fetched from the host store; see dd.h."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().dd_correct_misses(
+        ctypes.byref(shape.c()), _dev(q), _dev(k_dev), _dev(idx_spec), _dev(k_buf_spec),
+        _dev(v_buf_spec), _host(k_host), _host(v_host), _dev(idx_true_out), _dev(k_buf_out),
+        _dev(v_buf_out), _dev(miss_out), _dev(mass_out), _dev(workspace), ws_bytes,
+        _stream(stream)), "dd_correct_misses")
+
+
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -274,14 +292,16 @@ class Ctx:
         return arr
 
     def decode_step(self, layers, compute=None, copy=None, timing: bool = False,
-                    late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False):
+                    late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False,
+                    correct_misses: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
         flags = ((DD_STEP_TIMING if timing else 0) | (DD_STEP_LATE_GATHER if late_gather else 0)
                  | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
-                 | (DD_STEP_PIPELINE if pipeline else 0))
+                 | (DD_STEP_PIPELINE if pipeline else 0)
+                 | (DD_STEP_CORRECT_MISSES if correct_misses else 0))
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 
@@ -289,6 +309,17 @@ class Ctx:
         t = dd_phase_times()
         _check(_lib().dd_ctx_timings(self._h, ctypes.byref(t)), "dd_ctx_timings")
         return {f: getattr(t, f) for f, _ in dd_phase_times._fields_}
+
+    def correction_stats(self, n_layers: int):
+        """(misses [n_layers][units] int32, mass [n_layers][units][2] float32) of the
+        last step run with correct_misses=True."""
+        import numpy as np
+        U = self.shape.batch * self.shape.n_kv_heads
+        misses = np.zeros((n_layers, U), np.int32)
+        mass = np.zeros((n_layers, U, 2), np.float32)
+        _check(_lib().dd_ctx_correction_stats(self._h, misses.ctypes.data, mass.ctypes.data,
+                                              n_layers), "dd_ctx_correction_stats")
+        return misses, mass
 
     def score_times(self, n: int):
         buf = (ctypes.c_float * n)()

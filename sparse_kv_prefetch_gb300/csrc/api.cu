@@ -109,6 +109,8 @@ WsLayout ws_layout(const Dims& d) {
   off += align256((size_t)d.B * d.Hq * d.nsplit * d.d * sizeof(float));
   w.attn_ml = off;
   off += align256((size_t)d.B * d.Hq * d.nsplit * sizeof(float2));
+  w.sel_true = off;
+  off += align256((size_t)d.U * d.k * sizeof(float));
   w.total = off;
   return w;
 }
@@ -317,6 +319,44 @@ dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
+dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_dev,
+                            const int32_t* idx_spec, const void* k_buf_spec,
+                            const void* v_buf_spec, const void* k_host, const void* v_host,
+                            int32_t* idx_true_out, void* k_buf_out, void* v_buf_out,
+                            int32_t* miss_out, float* mass_out, void* workspace, size_t ws_bytes,
+                            dd_stream_t stream) {
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  if (d.k > kMaxCorrectK) return DD_ERR_UNSUPPORTED;
+  if (!q || !k_dev || !idx_spec || !k_buf_spec || !v_buf_spec || !k_host || !v_host ||
+      !idx_true_out || !k_buf_out || !v_buf_out || !workspace)
+    return DD_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_dev) || !aligned16(k_buf_spec) || !aligned16(v_buf_spec) ||
+      !aligned16(k_host) || !aligned16(v_host) || !aligned16(k_buf_out) ||
+      !aligned16(v_buf_out) || !aligned16(workspace))
+    return DD_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(d);
+  if (ws_bytes < w.total) return DD_ERR_INVALID_ARG;
+  const void* kh = host_to_device(k_host);
+  const void* vh = host_to_device(v_host);
+  if (!kh || !vh) return DD_ERR_INVALID_ARG;
+  if (!all_device({q, k_dev, idx_spec, k_buf_spec, v_buf_spec, idx_true_out, k_buf_out, v_buf_out,
+                   miss_out, mass_out, workspace}))
+    return DD_ERR_INVALID_ARG;
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  float* logits = reinterpret_cast<float*>(ws + w.logits);
+  float2* part = reinterpret_cast<float2*>(ws + w.part);
+  float* sel_true = reinterpret_cast<float*>(ws + w.sel_true);
+  st = cuda_status(launch_score(d, q, k_dev, logits, part, s));
+  if (st != DD_OK) return st;
+  st = cuda_status(launch_topk(d, logits, part, idx_true_out, sel_true, nullptr, s));
+  if (st != DD_OK) return st;
+  return cuda_status(launch_fixup(d, idx_spec, idx_true_out, sel_true, k_buf_spec, v_buf_spec, kh,
+                                  vh, k_buf_out, v_buf_out, miss_out, mass_out, s));
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------ context
@@ -342,6 +382,16 @@ struct dd_ctx {
   int timed_layers;
   int timed_launches;
   bool timed_serial;
+  // Miss correction (DD_STEP_CORRECT_MISSES): the real query's indices and
+  // rows, and per-layer statistics, grown to the largest layer count used.
+  int32_t* idx_true;
+  void* kb_true;
+  void* vb_true;
+  int32_t* miss;  // [layers][U]
+  float* mass;    // [layers][U][2]: predicted, total
+  int corr_layers;
+  int last_corr_layers;
+  cudaEvent_t ev_done;
 };
 
 namespace {
@@ -362,12 +412,46 @@ void ctx_free(dd_ctx* c) {
   }
   cudaFree(c->lse);
   cudaFree(c->ws);
+  cudaFree(c->idx_true);
+  cudaFree(c->kb_true);
+  cudaFree(c->vb_true);
+  cudaFree(c->miss);
+  cudaFree(c->mass);
+  if (c->ev_done) cudaEventDestroy(c->ev_done);
   if (c->ev_join) cudaEventDestroy(c->ev_join);
   for (cudaEvent_t e : c->tev) cudaEventDestroy(e);
   if (c->t_begin) cudaEventDestroy(c->t_begin);
   if (c->t_end) cudaEventDestroy(c->t_end);
   if (prev >= 0) cudaSetDevice(prev);
   delete c;
+}
+
+dd_status ensure_correction_buffers(dd_ctx* c, int n_layers) {
+  const Dims& d = c->dims;
+  if (!c->idx_true) {
+    const size_t rows_bytes = (size_t)d.U * d.k * d.d * d.elt;
+    if (cudaMalloc((void**)&c->idx_true, (size_t)d.U * d.k * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&c->kb_true, rows_bytes) != cudaSuccess ||
+        cudaMalloc(&c->vb_true, rows_bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return DD_ERR_OOM;
+    }
+    c->device_bytes += (size_t)d.U * d.k * sizeof(int32_t) + 2 * rows_bytes;
+  }
+  if (n_layers > c->corr_layers) {
+    cudaFree(c->miss);
+    cudaFree(c->mass);
+    c->miss = nullptr;
+    c->mass = nullptr;
+    if (cudaMalloc((void**)&c->miss, (size_t)n_layers * d.U * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc((void**)&c->mass, (size_t)n_layers * d.U * 2 * sizeof(float)) != cudaSuccess) {
+      cudaGetLastError();
+      c->corr_layers = 0;
+      return DD_ERR_OOM;
+    }
+    c->corr_layers = n_layers;
+  }
+  return DD_OK;
 }
 
 dd_status ensure_timing_events(dd_ctx* c, int n_layers) {
@@ -425,6 +509,7 @@ dd_status dd_ctx_create(const dd_shape* shape, dd_ctx** out) {
          cudaEventCreateWithFlags(&c->ev_ready[i], cudaEventDisableTiming) == cudaSuccess &&
          cudaEventCreateWithFlags(&c->ev_free[i], cudaEventDisableTiming) == cudaSuccess;
   ok = ok && cudaEventCreateWithFlags(&c->ev_join, cudaEventDisableTiming) == cudaSuccess;
+  ok = ok && cudaEventCreateWithFlags(&c->ev_done, cudaEventDisableTiming) == cudaSuccess;
   if (!ok) {
     ctx_free(c);
     return DD_ERR_CUDA;
@@ -459,6 +544,13 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   }
   const bool timing = (flags & DD_STEP_TIMING) != 0;
   const int gather_mode = (flags & DD_STEP_GATHER_LSU) ? 1 : 0;
+  const bool correct = (flags & DD_STEP_CORRECT_MISSES) != 0;
+  if (correct) {
+    if (d.k > kMaxCorrectK) return DD_ERR_UNSUPPORTED;
+    if ((flags & DD_STEP_PIPELINE) && copy && copy != compute) return DD_ERR_UNSUPPORTED;
+    dd_status st = ensure_correction_buffers(c, n_layers);
+    if (st != DD_OK) return st;
+  }
   if (timing) {
     dd_status st = ensure_timing_events(c, n_layers);
     if (st != DD_OK) return st;
@@ -522,8 +614,24 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       if (e != cudaSuccess) return e;
     }
     if (timing) cudaEventRecord(T(l, PH_ATTN0), A);
-    e = launch_attn(d, layers[l].q, c->kbuf[s], c->vbuf[s], layers[l].k_dev, layers[l].v_win,
-                    layers[l].out, attn_o, attn_ml, A);
+    const void* kb = c->kbuf[s];
+    const void* vb = c->vbuf[s];
+    if (correct) {
+      // The real query's own top-k; rows the prediction missed come from host.
+      float* sel_true = reinterpret_cast<float*>(ws + c->ws_lay.sel_true);
+      e = launch_score(d, layers[l].q, layers[l].k_dev, logits, part, A);
+      if (e == cudaSuccess) e = launch_topk(d, logits, part, c->idx_true, sel_true, nullptr, A);
+      if (e == cudaSuccess)
+        e = launch_fixup(d, c->idx[s], c->idx_true, sel_true, c->kbuf[s], c->vbuf[s], kh[l], vh[l],
+                         c->kb_true, c->vb_true, c->miss + (size_t)l * d.U,
+                         c->mass + (size_t)l * d.U * 2, A);
+      if (e != cudaSuccess) return e;
+      launches += kScoreLaunches + kTopkLaunches + kFixupLaunches;
+      kb = c->kb_true;
+      vb = c->vb_true;
+    }
+    e = launch_attn(d, layers[l].q, kb, vb, layers[l].k_dev, layers[l].v_win, layers[l].out,
+                    attn_o, attn_ml, A);
     if (e != cudaSuccess) return e;
     if (timing) cudaEventRecord(T(l, PH_ATTN1), A);
     launches += kAttnLaunches;
@@ -575,6 +683,8 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     DD_TRY(cudaEventRecord(c->ev_join, X));
     DD_TRY(cudaStreamWaitEvent(C, c->ev_join, 0));
   }
+  DD_TRY(cudaEventRecord(c->ev_done, C));
+  if (correct) c->last_corr_layers = n_layers;
   if (timing) {
     DD_TRY(cudaEventRecord(c->t_end, C));
     c->timed_layers = n_layers;
@@ -607,6 +717,20 @@ dd_status dd_ctx_timings(dd_ctx* c, dd_phase_times* out) {
   }
   out->n_layers = c->timed_layers;
   out->launches = c->timed_launches;
+  return DD_OK;
+}
+
+dd_status dd_ctx_correction_stats(dd_ctx* c, int32_t* misses, float* mass, int n_layers) {
+  if (!c || n_layers < 0) return DD_ERR_INVALID_ARG;
+  if (c->last_corr_layers <= 0 || n_layers > c->last_corr_layers) return DD_ERR_INVALID_ARG;
+  if (cudaEventSynchronize(c->ev_done) != cudaSuccess) return DD_ERR_CUDA;
+  const size_t U = (size_t)c->dims.U;
+  if (misses && cudaMemcpy(misses, c->miss, (size_t)n_layers * U * sizeof(int32_t),
+                           cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DD_ERR_CUDA;
+  if (mass && cudaMemcpy(mass, c->mass, (size_t)n_layers * U * 2 * sizeof(float),
+                         cudaMemcpyDeviceToHost) != cudaSuccess)
+    return DD_ERR_CUDA;
   return DD_OK;
 }
 

@@ -23,7 +23,7 @@ struct Dims {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t logits, part, attn_o, attn_ml, total;
+  size_t logits, part, attn_o, attn_ml, sel_true, total;
 };
 
 dd_status resolve(const dd_shape* s, Dims* out);
@@ -44,8 +44,17 @@ cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const v
                         const void* k_dev, const void* v_win, float* out, float* part_o,
                         float2* part_ml, cudaStream_t st);
 
+// Miss correction (correct.cu): copy each row of the real query's top-k from
+// the prefetched buffer, or from the host store where the prediction missed.
+constexpr int kMaxCorrectK = 4096;
+cudaError_t launch_fixup(const Dims& d, const int32_t* idx_spec, const int32_t* idx_true,
+                         const float* sel_true, const void* kb_spec, const void* vb_spec,
+                         const void* k_host, const void* v_host, void* kb_out, void* vb_out,
+                         int32_t* miss_out, float* mass_out, cudaStream_t st);
+
 // Number of kernels each launcher enqueues.
-constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 2, kAttnLaunches = 2;
+constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 2, kAttnLaunches = 2,
+              kFixupLaunches = 1;
 
 // Huge-page size of the host (transparent huge pages), read once; 2 MiB if
 // the host does not report one.  Host stores from dd_host_alloc use it.
