@@ -104,6 +104,14 @@ def barrier(world):
         dist.barrier()
 
 
+def job_throughput(layers_per_rank_step: int, steps: int, seconds_per_rank: float,
+                   world: int) -> float:
+    """Whole-job layer-steps/s: every rank runs its own replica (independent
+    requests), so the job processes world x layers x steps layer-steps in the
+    slowest rank's time (the caller passes the max over ranks)."""
+    return world * layers_per_rank_step * steps / seconds_per_rank
+
+
 def max_over_ranks(x: float, world: int) -> float:
     if world == 1:
         return x
@@ -397,7 +405,7 @@ def run_ours(args, rank, world):
     clk = clocks.stop()
     total_s = ev0.elapsed_time(ev1) * 1e-3
     total_s = max_over_ranks(total_s, world)
-    value = world * L * args.steps / total_s
+    value = job_throughput(L, args.steps, total_s, world)
 
     # Serial schedule (same work, one stream) for the hidden fraction.
     serial = [step(None) for _ in range(max(3, args.steps // 4))]
@@ -434,7 +442,7 @@ def run_ours(args, rank, world):
     e1.record(compute)
     torch.cuda.synchronize()
     e2e_s = max_over_ranks(e0.elapsed_time(e1) * 1e-3, world)
-    e2e_value = world * L * e2e_steps / e2e_s
+    e2e_value = job_throughput(L, e2e_steps, e2e_s, world)
     if not torch.equal(out_h.to(dev), outs):
         raise RuntimeError("e2e read-back differs from the device outputs")
 
