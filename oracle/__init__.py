@@ -95,8 +95,12 @@ class Oracle:
         L.orc_dense_unit.argtypes = [S, _P, _P, _P, ctypes.c_int, ctypes.c_int, _D]
         L.orc_layer.argtypes = [S, _P, _P, _P, _P, _I, _D, _D, _D, _D, ctypes.c_int64,
                                 ctypes.c_int64, ctypes.c_int]
+        L.orc_landmarks_unit.argtypes = [S, ctypes.c_int, _P, ctypes.c_int, ctypes.c_int, _D]
+        L.orc_landmark_select_unit.argtypes = [S, ctypes.c_int, _P, _D, ctypes.c_int, ctypes.c_int,
+                                               _I, _D, _D, _D]
         for f in ("orc_score_unit", "orc_selection_score", "orc_select_unit",
-                  "orc_attend_unit", "orc_dense_unit", "orc_layer"):
+                  "orc_attend_unit", "orc_dense_unit", "orc_layer", "orc_landmarks_unit",
+                  "orc_landmark_select_unit"):
             getattr(L, f).restype = None
 
     # -- steps 1-2 ---------------------------------------------------------
@@ -144,6 +148,29 @@ class Oracle:
         self.lib.orc_dense_unit(ctypes.byref(s.c()), _ptr(q), _ptr(K), _ptr(V), b, hk,
                                 out.ctypes.data_as(_D))
         return out
+
+    # -- landmark (chunk) selection ----------------------------------------
+    def landmarks_unit(self, s: Shape, chunk: int, K, b: int, hk: int) -> np.ndarray:
+        """Landmarks [M][d] of unit (b, hk): the mean key of each chunk of
+        [0, n - W)."""
+        M = (s.ctx_len - s.window) // chunk
+        L = np.empty((M, s.head_dim), np.float64)
+        self.lib.orc_landmarks_unit(ctypes.byref(s.c()), chunk, _ptr(K), b, hk,
+                                    L.ctypes.data_as(_D))
+        return L
+
+    def landmark_select_unit(self, s: Shape, chunk: int, q_spec, L: np.ndarray, b: int, hk: int):
+        """(rows [k] ascending, chunk scores [k/c], chunk LSE [G], gap) of unit (b, hk)."""
+        L = np.ascontiguousarray(L, np.float64)
+        rows = np.empty(s.top_k, np.int32)
+        sel = np.empty(s.top_k // chunk, np.float64)
+        lse = np.empty(s.group, np.float64)
+        gap = ctypes.c_double()
+        self.lib.orc_landmark_select_unit(ctypes.byref(s.c()), chunk, _ptr(q_spec),
+                                          L.ctypes.data_as(_D), b, hk, rows.ctypes.data_as(_I),
+                                          sel.ctypes.data_as(_D), lse.ctypes.data_as(_D),
+                                          ctypes.byref(gap))
+        return rows, sel, lse, gap.value
 
     # -- whole layer -------------------------------------------------------
     def layer(self, s: Shape, q_spec, q, K, V, nthreads: int = 1, units=None):

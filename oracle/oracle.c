@@ -239,3 +239,78 @@ void orc_layer(const orc_shape* s, const void* q_spec, const void* q, const void
   for (int t = 0; t < nthreads; ++t)
     if (live[t]) pthread_join(th[t], NULL);
 }
+
+/* ---------------- landmark (chunk) selection ----------------
+ *
+ * The DualDecoder paper (Sec. 1) computes the retrieval index from the token
+ * being processed and static GPU-resident KV landmarks; Sec. 2.2 describes
+ * chunks of adjacent KV entries, each with a compressed landmark, the GPU
+ * selecting chunks for the current query and retrieving their entries.  The
+ * landmark itself is not specified; here it is the mean of the chunk's keys.
+ * With chunk size c, the candidate positions [0, n - W) form M = (n - W) / c
+ * chunks (c divides n - W and k):
+ *   L_m   = (1/c) sum_{r < c} K[m c + r]                       (landmark)
+ *   s_h,m = q_spec[h] . L_m / sqrt(d_k), alpha_h = softmax over m
+ *   a_m   = alpha_m (MHA) or sum over the group of alpha_h,m
+ *   the k / c chunks with the largest a_m (ties to the lower m) are selected,
+ *   and the selected rows are every position of those chunks, ascending.
+ */
+
+/* Landmarks of unit (b, hk): L is [M][d]. */
+void orc_landmarks_unit(const orc_shape* s, int chunk, const void* K, int b, int hk, double* L) {
+  const int d = s->head_dim, n = s->ctx_len, M = (s->ctx_len - s->window) / chunk;
+  const int64_t row0 = ((int64_t)b * s->n_kv_heads + hk) * n;
+  for (int m = 0; m < M; ++m)
+    for (int t = 0; t < d; ++t) {
+      double acc = 0.0;
+      for (int r = 0; r < chunk; ++r) acc += widen(K, s->dtype, (row0 + (int64_t)m * chunk + r) * d + t);
+      L[(int64_t)m * d + t] = acc / chunk;
+    }
+}
+
+/*
+ * Chunk selection of unit (b, hk) from its landmarks L ([M][d]).  Writes the
+ * k selected rows (ascending) to rows, the selected chunks' scores a_m to
+ * sel ([k / c], ascending chunk order, may be NULL), the chunks' LSE per query
+ * head of the group to lse ([G], may be NULL) and the relative gap between the
+ * (k/c)-th and (k/c + 1)-th chunk score to *gap (may be NULL).
+ */
+void orc_landmark_select_unit(const orc_shape* s, int chunk, const void* q_spec, const double* L,
+                              int b, int hk, int32_t* rows, double* sel, double* lse, double* gap) {
+  const int G = group_size(s), d = s->head_dim, M = (s->ctx_len - s->window) / chunk;
+  const int kc = s->top_k / chunk;
+  const double inv_sqrt_d = 1.0 / sqrt((double)d);
+  double* lg = (double*)malloc(sizeof(double) * (size_t)M);
+  double* a = (double*)calloc((size_t)M, sizeof(double));
+  for (int g = 0; g < G; ++g) {
+    const int h = hk * G + g;
+    const int64_t q_off = ((int64_t)b * s->n_q_heads + h) * d;
+    double mx = -INFINITY;
+    for (int m = 0; m < M; ++m) {
+      double acc = 0.0;
+      for (int t = 0; t < d; ++t) acc += widen(q_spec, s->dtype, q_off + t) * L[(int64_t)m * d + t];
+      lg[m] = acc * inv_sqrt_d;
+      if (lg[m] > mx) mx = lg[m];
+    }
+    double sum = 0.0;
+    for (int m = 0; m < M; ++m) sum += exp(lg[m] - mx);
+    const double l = mx + log(sum);
+    if (lse) lse[g] = l;
+    for (int m = 0; m < M; ++m) a[m] += exp(lg[m] - l);
+  }
+  cand* c = (cand*)malloc(sizeof(cand) * (size_t)M);
+  for (int m = 0; m < M; ++m) {
+    c[m].a = a[m];
+    c[m].j = m;
+  }
+  qsort(c, (size_t)M, sizeof(cand), by_score_desc);
+  if (gap) *gap = (kc < M) ? (c[kc - 1].a - c[kc].a) / c[kc - 1].a : INFINITY;
+  qsort(c, (size_t)kc, sizeof(cand), by_index_asc);
+  for (int i = 0; i < kc; ++i) {
+    if (sel) sel[i] = c[i].a;
+    for (int r = 0; r < chunk; ++r) rows[i * chunk + r] = c[i].j * chunk + r;
+  }
+  free(c);
+  free(a);
+  free(lg);
+}

@@ -300,4 +300,73 @@ def pin_attention_window_only(orc):
     assert not np.array_equal(orc.attend_unit(s, q, K, V3, 0, 0, np.zeros(0, np.int32), True), base)
 
 
+# --------------------------------------------------------------------------
+# landmark (chunk) selection
+# --------------------------------------------------------------------------
+
+def pin_landmarks_chunk1_is_plain_topk(orc):
+    """With one position per chunk the landmark is the key itself, so chunk
+    selection must reproduce the (separately pinned) plain top-k: the same rows,
+    for MHA and for a GQA group.  Without a window the chunk softmax covers the
+    same positions as the plain one, so the scores and LSE agree too (with a
+    window the chunks exclude it and the normalisation differs)."""
+    for (B, Hq, Hkv, d, n, k, W, dt) in [(2, 2, 2, 8, 90, 9, 5, F32), (1, 8, 2, 16, 70, 6, 0, BF16)]:
+        s = Shape(B, Hq, Hkv, d, n, k, W, dt)
+        q, K, _ = _attn_case(B, Hq, Hkv, d, n, W, dt, 51)
+        for b in range(B):
+            for hk in range(Hkv):
+                L = orc.landmarks_unit(s, 1, K, b, hk)
+                Kf = K if dt == F32 else synth.bf16_bits_to_f32(K)
+                assert np.array_equal(L, Kf[b, hk, : n - W].astype(np.float64))
+                rows, sel, lse, gap = orc.landmark_select_unit(s, 1, q, L, b, hk)
+                lg, lse0 = orc.score_unit(s, q, K, b, hk)
+                a = orc.selection_score(s, lg, lse0)
+                idx, sel0, gap0 = orc.select_unit(s, a)
+                assert rows.tolist() == idx.tolist()
+                if W == 0:
+                    np.testing.assert_allclose(sel, sel0, rtol=1e-12)
+                    np.testing.assert_allclose(lse, lse0, rtol=1e-12)
+
+
+def pin_landmark_is_chunk_mean(orc):
+    """Keys j * e_t (an arithmetic run) have the closed-form chunk mean
+    (m c + (c - 1)/2) e_t; positions of the window form no chunk."""
+    B, Hq, Hkv, d, n, W, c = 2, 2, 2, 4, 48, 8, 8
+    s = Shape(B, Hq, Hkv, d, n, 8, W, F32)
+    K = np.zeros((B, Hkv, n, d), np.float32)
+    for b in range(B):
+        for hk in range(Hkv):
+            K[b, hk, :, (b + 2 * hk) % d] = np.arange(n) * (1 + hk + b)
+    for b in range(B):
+        for hk in range(Hkv):
+            L = orc.landmarks_unit(s, c, K, b, hk)
+            assert L.shape == ((n - W) // c, d)
+            for m in range(L.shape[0]):
+                want = np.zeros(d)
+                want[(b + 2 * hk) % d] = (m * c + (c - 1) / 2) * (1 + hk + b)
+                assert np.array_equal(L[m], want)
+
+
+def pin_landmark_selection_by_hand(orc):
+    """Chunks of equal keys v_m e_1 and q = (x, 0) give chunk logits x v_m / sqrt 2:
+    the chunks with the largest v_m win, ties to the lower chunk, and each
+    selected chunk contributes all of its positions."""
+    d, c, W = 2, 4, 3
+    v = [1.0, 5.0, 2.0, 5.0, 0.5, 4.0, 5.0]  # 7 chunks, a three-way tie at 5
+    n = len(v) * c + W
+    for kc, want_chunks in [(1, [1]), (2, [1, 3]), (3, [1, 3, 6]), (4, [1, 3, 5, 6])]:
+        s = Shape(1, 1, 1, d, n, kc * c, W, F32)
+        K = np.zeros((1, 1, n, d), np.float32)
+        for m, vm in enumerate(v):
+            K[0, 0, m * c:(m + 1) * c, 0] = vm
+        K[0, 0, n - W:, 0] = 100.0  # the window never competes
+        q = np.array([[[0.7, 0.0]]], np.float32)
+        L = orc.landmarks_unit(s, c, K, 0, 0)
+        rows, sel, lse, gap = orc.landmark_select_unit(s, c, q, L, 0, 0)
+        assert rows.tolist() == [m * c + r for m in want_chunks for r in range(c)], (kc, rows)
+        lg = np.array([float(np.float32(0.7)) * vm / math.sqrt(2.0) for vm in v])
+        al = np.exp(lg - lg.max()) / np.exp(lg - lg.max()).sum()
+        np.testing.assert_allclose(sel, al[want_chunks], rtol=1e-12)
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -45,6 +45,15 @@ MUTANTS = [
      "e[r] = dot_row(s, q, q_off, K, (unit_row0 + j) * d);"),
     ("attn_drop_window", "const int64_t n_win = include_window ? s->window : 0;",
      "const int64_t n_win = 0;"),
+    ("landmark_mean_denominator", "L[(int64_t)m * d + t] = acc / chunk;",
+     "L[(int64_t)m * d + t] = acc / (chunk + 1);"),
+    ("landmark_row_stride", "acc += widen(K, s->dtype, (row0 + (int64_t)m * chunk + r) * d + t);",
+     "acc += widen(K, s->dtype, (row0 + (int64_t)m + r) * d + t);"),
+    ("landmark_rows_shifted", "rows[i * chunk + r] = c[i].j * chunk + r;",
+     "rows[i * chunk + r] = c[i].j * chunk + r + 1;"),
+    ("landmark_first_head_only", "for (int m = 0; m < M; ++m) a[m] += exp(lg[m] - l);",
+     "if (g == 0) for (int m = 0; m < M; ++m) a[m] += exp(lg[m] - l);"),
+    ("landmark_no_scale", "lg[m] = acc * inv_sqrt_d;", "lg[m] = acc;"),
 ]
 
 
