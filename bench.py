@@ -65,6 +65,9 @@ def parse():
                         "copy stream")
     p.add_argument("--correct-misses", action="store_true",
                    help="correct prediction misses in every timed layer (DD_STEP_CORRECT_MISSES)")
+    p.add_argument("--landmarks", type=int, default=0, metavar="C",
+                   help="select whole chunks of C rows by their mean-key landmarks "
+                        "(DD_STEP_LANDMARKS) instead of scoring every key; 0: off")
     p.add_argument("--late-gather", type=int, default=0,
                    help="1: start each layer's gather after the previous attention")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -231,7 +234,8 @@ def config_of(w, args):
             "gather_mode": ["bulk_copy", "load_store"][args.gather_mode],
             "host_store": args.host_alloc, "schedule": args.schedule,
             "copy_stream_priority": args.copy_priority,
-            "correct_misses": bool(args.correct_misses)}
+            "correct_misses": bool(args.correct_misses),
+            "landmark_chunk": args.landmarks or None}
 
 
 def run_reference(args, rank, world):
@@ -301,8 +305,17 @@ def run_ours(args, rank, world):
         compute, copy = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
     else:
         compute, copy = torch.cuda.Stream(priority=-1), torch.cuda.Stream()
+    C = args.landmarks
+    lm_d = None
+    if C:  # chunk landmarks of every layer slot, built once (prefill-time work)
+        M = (n - W) // C
+        lm_d = torch.empty((D, B, Hkv, M, d), dtype=torch.float32, device=dev)
+        for s_ in range(D):
+            dd.build_landmarks(shape, C, K_d[s_], lm_d[s_])
+        ctx.set_landmark_chunk(C)
     layers = dd.Ctx.pack([dd.LayerIO(qs_d[l % D], q_d[l % D], K_d[l % D], K_h[l % D],
-                                     V_h[l % D], vwin_d[l % D] if W > 0 else None, outs[l])
+                                     V_h[l % D], vwin_d[l % D] if W > 0 else None, outs[l],
+                                     lm_d[l % D] if C else None)
                           for l in range(L)])
     torch.cuda.synchronize()
 
@@ -331,8 +344,16 @@ def run_ours(args, rank, world):
     g_ws = torch.empty(dd.workspace_size(shape), dtype=torch.uint8, device=dev)
     g_kb = torch.empty((U, k, d), dtype=dt, device=dev)
     g_vb = torch.empty_like(g_kb)
+    if C:
+        lm_ws = torch.empty(dd.landmarks_workspace_size(shape, C), dtype=torch.uint8, device=dev)
+        g_csel = torch.empty((U, k // C), dtype=torch.float32, device=dev)
     for s_ in range(D):
-        dd.score_topk(shape, qs_d[s_], K_d[s_], g_idx[s_], g_sel, g_lse, g_ws, stream=compute)
+        if C:
+            dd.score_topk_landmarks(shape, C, qs_d[s_], lm_d[s_], g_idx[s_], g_csel,
+                                    g_lse, lm_ws, stream=compute)
+        else:
+            dd.score_topk(shape, qs_d[s_], K_d[s_], g_idx[s_], g_sel, g_lse, g_ws,
+                          stream=compute)
     gather_alone = {}
     for mode in (0, 1):
         for i in range(2 * D):
@@ -370,15 +391,17 @@ def run_ours(args, rank, world):
             "recall": float(1.0 - pm.mean() / k),
             "recall_min_unit": float(1.0 - pm.max() / k),
             "mass_recall": float(ms[..., 0].sum() / ms[..., 1].sum()),
-            "what": "|TopK(q_spec) & TopK(q)| / k and the real query's selection score "
-                    "captured by the prefetched rows, over all layer slots and units",
+            "what": ("|TopK(q_spec) & TopK(q)| / k" if not C else
+                     "|chunk rows selected with q_spec & TopK(q)| / k")
+                    + " and the real query's selection score captured by the prefetched rows,"
+                      " over all layer slots and units",
         }
     del g_ws, g_kb, g_vb
 
     def step(copy_stream, timing=True):
         ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
                         late_gather=late, pipeline=pipe, gather_mode=args.gather_mode,
-                        correct_misses=args.correct_misses)
+                        correct_misses=args.correct_misses, landmarks=bool(C))
         return ctx.timings() if timing else None
 
     compute.wait_stream(torch.cuda.current_stream())
@@ -419,7 +442,8 @@ def run_ours(args, rank, world):
     qs_src = torch.stack([qs_h[l % D] for l in range(L)]).pin_memory()
     q_src = torch.stack([q_h[l % D] for l in range(L)]).pin_memory()
     layers_e2e = dd.Ctx.pack([dd.LayerIO(qs_l[l], q_l[l], K_d[l % D], K_h[l % D], V_h[l % D],
-                                         vwin_d[l % D] if W > 0 else None, outs[l])
+                                         vwin_d[l % D] if W > 0 else None, outs[l],
+                                         lm_d[l % D] if C else None)
                               for l in range(L)])
     e2e_steps = max(3, args.steps // 2)
 
@@ -428,7 +452,8 @@ def run_ours(args, rank, world):
             qs_l.copy_(qs_src, non_blocking=True)
             q_l.copy_(q_src, non_blocking=True)
         ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=late, pipeline=pipe,
-                        gather_mode=args.gather_mode, correct_misses=args.correct_misses)
+                        gather_mode=args.gather_mode, correct_misses=args.correct_misses,
+                        landmarks=bool(C))
         with torch.cuda.stream(compute):
             out_h.copy_(outs, non_blocking=True)
     for _ in range(2):
@@ -448,6 +473,8 @@ def run_ours(args, rank, world):
 
     # Derived rates.
     k_bytes, g_bytes = w.k_bytes(), w.gather_bytes()
+    if C:  # the scoring phase reads the fp32 landmarks instead of K
+        k_bytes = U * ((n - W) // C) * d * 4
     score_mean_ms = statistics.mean(score_ms)
     score_gbs = k_bytes / (score_mean_ms * 1e-3) / 1e9
     gather_ms_layer = statistics.mean(p["gather_ms"] for p in phases) / L
@@ -494,10 +521,13 @@ def run_ours(args, rank, world):
         "serial_phase_ms_per_step": {kk: statistics.mean(p[kk] for p in serial)
                                      for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms",
                                                 "attn_ms")},
-        "roofline": {"bound": "hbm", "kernel": "score_kernel", "achieved": score_gbs,
+        "roofline": {"bound": "hbm",
+                     "kernel": ("score_kernel" if not C else
+                                "landmark selection phase (widen q, score, top-k, expand)"),
+                     "achieved": score_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": score_gbs / peak,
-                     "traffic": (None if args.profile_case
+                     "traffic": (None if args.profile_case or C
                                  else SCORE_TRAFFIC_BYTES.get(w.name)),
                      "algorithmic_bytes_per_launch": k_bytes},
         "cpu_baseline": cpu,

@@ -251,6 +251,46 @@ dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_
                             int32_t* miss_out, float* mass_out, void* workspace, size_t ws_bytes,
                             dd_stream_t stream);
 
+/* ------------------------ landmark selection ------------------------ */
+
+/*
+ * Chunk landmarks (DualDecoder paper, Sec. 1: the retrieval index is computed
+ * from the current token and static GPU-resident KV landmarks; Sec. 2.2:
+ * adjacent KV entries are grouped into chunks with compressed landmarks, the
+ * GPU picks chunks for the current query and fetches their entries from host
+ * memory).  The paper does not define the landmark; here it is the mean key
+ * of each chunk of c adjacent positions of [0, n - W), in fp32:
+ *   landmarks[u][m][t] = (1/c) sum_{r<c} K[u][m c + r][t],  M = (n - W) / c.
+ * Constraints: c >= 2, c divides n - W and k, d in {64, 128}; otherwise
+ * DD_ERR_UNSUPPORTED.
+ */
+dd_status dd_landmarks_size(const dd_shape* shape, int chunk, size_t* bytes);
+
+/*
+ * Build the landmarks of one layer's keys (device k_dev [B][H_kv][n][d] of the
+ * shape's dtype) into device landmarks_out [B][H_kv][M][d] fp32.  Built once
+ * per prefill: the keys of [0, n - W) do not change while decoding.
+ */
+dd_status dd_build_landmarks(const dd_shape* shape, int chunk, const void* k_dev,
+                             float* landmarks_out, dd_stream_t stream);
+
+/*
+ * Landmark selection: score q_spec against the M landmarks exactly as
+ * dd_score_topk scores keys (fp32 arithmetic; bf16 queries are widened first),
+ * with no window, take each unit's top k/c chunks (ties to the lower chunk,
+ * ascending), and write their k rows in ascending order:
+ *   idx_out          device [B][H_kv][k] int32, chunk m -> rows m c .. m c + c - 1
+ *   chunk_score_out  device [B][H_kv][k/c] f32, the chunk's selection score
+ *                    (softmax over chunks, summed over the group's heads)
+ *   lse_out          device [B][H_q] f32 over the chunk logits, or NULL
+ * The workspace must hold dd_landmarks_workspace_size bytes.
+ */
+dd_status dd_landmarks_workspace_size(const dd_shape* shape, int chunk, size_t* bytes);
+dd_status dd_score_topk_landmarks(const dd_shape* shape, int chunk, const void* q_spec,
+                                  const float* landmarks, int32_t* idx_out, float* chunk_score_out,
+                                  float* lse_out, void* workspace, size_t ws_bytes,
+                                  dd_stream_t stream);
+
 /* ---------------------------- layer loop ---------------------------- */
 
 typedef struct dd_ctx dd_ctx;
@@ -264,6 +304,8 @@ typedef struct {
   const void* v_host; /* pinned host [B][H_kv][n][d] */
   const void* v_win;  /* device [B][H_kv][W][d] (NULL if W = 0) */
   float* out;         /* device [B][H_q][d] */
+  const float* landmarks; /* device [B][H_kv][(n-W)/c][d] fp32 from dd_build_landmarks;
+                             read only under DD_STEP_LANDMARKS (else may be NULL) */
 } dd_layer_io;
 
 /*
@@ -290,12 +332,23 @@ enum {
                               (dd_correct_misses; k <= 4096; not combinable with
                               DD_STEP_PIPELINE); statistics via
                               dd_ctx_correction_stats */
-  DD_STEP_PIPELINE = 8     /* two-stage pipeline: scoring and top-k of every
+  DD_STEP_PIPELINE = 8,    /* two-stage pipeline: scoring and top-k of every
                               layer on `compute`; the gather and then the
                               attention of each layer on `copy`, as soon as its
                               indices are ready (compute runs at most two layers
                               ahead); attention never runs beside a gather */
+  DD_STEP_LANDMARKS = 32   /* select with dd_score_topk_landmarks over each
+                              layer's `landmarks` instead of scoring every key
+                              (chunk set by dd_ctx_set_landmark_chunk; not
+                              combinable with DD_STEP_CORRECT_MISSES) */
 };
+
+/*
+ * Landmark chunk size for DD_STEP_LANDMARKS.  Allocates the context's landmark
+ * workspace on first use (or when a larger one is needed; then it first waits
+ * for the device).  Same constraints as dd_score_topk_landmarks.
+ */
+dd_status dd_ctx_set_landmark_chunk(dd_ctx* ctx, int chunk);
 
 /*
  * Enqueue one decode step over n_layers layers.  Steps 1-2 of layer l+1 run

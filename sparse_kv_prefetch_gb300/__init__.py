@@ -27,6 +27,7 @@ DD_STEP_LATE_GATHER = 2
 DD_STEP_GATHER_LSU = 4
 DD_STEP_PIPELINE = 8
 DD_STEP_CORRECT_MISSES = 16
+DD_STEP_LANDMARKS = 32
 
 
 class DDError(RuntimeError):
@@ -43,7 +44,8 @@ class dd_shape(ctypes.Structure):
 class dd_layer_io(ctypes.Structure):
     _fields_ = [("q_spec", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k_dev", ctypes.c_void_p),
                 ("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p),
-                ("v_win", ctypes.c_void_p), ("out", ctypes.c_void_p)]
+                ("v_win", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("landmarks", ctypes.c_void_p)]
 
 
 class dd_phase_times(ctypes.Structure):
@@ -104,6 +106,14 @@ def _lib():
             "dd_correct_misses": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
                                   ctypes.c_int),
             "dd_ctx_correction_stats": ([P, P, P, ctypes.c_int], ctypes.c_int),
+            "dd_landmarks_size": ([S, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+                                  ctypes.c_int),
+            "dd_landmarks_workspace_size": ([S, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
+                                            ctypes.c_int),
+            "dd_build_landmarks": ([S, ctypes.c_int, P, P, P], ctypes.c_int),
+            "dd_score_topk_landmarks": ([S, ctypes.c_int, P, P, P, P, P, P, ctypes.c_size_t, P],
+                                        ctypes.c_int),
+            "dd_ctx_set_landmark_chunk": ([P, ctypes.c_int], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -234,6 +244,38 @@ def correct_misses(shape: Shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, k_h
         _stream(stream)), "dd_correct_misses")
 
 
+def landmarks_size(shape: Shape, chunk: int) -> int:
+    """Bytes of one layer's chunk landmarks (fp32 [B][H_kv][(n-W)/chunk][d])."""
+    n = ctypes.c_size_t()
+    _check(_lib().dd_landmarks_size(ctypes.byref(shape.c()), chunk, ctypes.byref(n)),
+           "dd_landmarks_size")
+    return n.value
+
+
+def landmarks_workspace_size(shape: Shape, chunk: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib().dd_landmarks_workspace_size(ctypes.byref(shape.c()), chunk, ctypes.byref(n)),
+           "dd_landmarks_workspace_size")
+    return n.value
+
+
+def build_landmarks(shape: Shape, chunk: int, k_dev, landmarks_out, stream=None):
+    """Chunk-mean landmarks of one layer's keys; see dd.h."""
+    _check(_lib().dd_build_landmarks(ctypes.byref(shape.c()), chunk, _dev(k_dev),
+                                     _dev(landmarks_out), _stream(stream)), "dd_build_landmarks")
+
+
+def score_topk_landmarks(shape: Shape, chunk: int, q_spec, landmarks, idx_out, chunk_score_out,
+                         lse_out, workspace, stream=None, ws_bytes: Optional[int] = None):
+    """Landmark selection: top k/chunk chunks per KV head, expanded to k rows; see dd.h."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().dd_score_topk_landmarks(ctypes.byref(shape.c()), chunk, _dev(q_spec),
+                                          _dev(landmarks), _dev(idx_out), _dev(chunk_score_out),
+                                          _dev(lse_out), _dev(workspace), ws_bytes,
+                                          _stream(stream)), "dd_score_topk_landmarks")
+
+
 NOALLOC_SCRATCH_BYTES = 32 << 20
 
 
@@ -255,6 +297,7 @@ class LayerIO(NamedTuple):
     v_host: object
     v_win: object
     out: object
+    landmarks: object = None
 
 
 class Ctx:
@@ -288,12 +331,17 @@ class Ctx:
         arr = (dd_layer_io * len(layers))()
         for i, io in enumerate(layers):
             arr[i] = dd_layer_io(_dev(io.q_spec), _dev(io.q), _dev(io.k_dev), _host(io.k_host),
-                                 _host(io.v_host), _dev(io.v_win), _dev(io.out))
+                                 _host(io.v_host), _dev(io.v_win), _dev(io.out),
+                                 _dev(io.landmarks))
         return arr
+
+    def set_landmark_chunk(self, chunk: int):
+        """Chunk size of landmark selection (decode_step(landmarks=True))."""
+        _check(_lib().dd_ctx_set_landmark_chunk(self._h, chunk), "dd_ctx_set_landmark_chunk")
 
     def decode_step(self, layers, compute=None, copy=None, timing: bool = False,
                     late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False,
-                    correct_misses: bool = False):
+                    correct_misses: bool = False, landmarks: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
@@ -301,7 +349,8 @@ class Ctx:
         flags = ((DD_STEP_TIMING if timing else 0) | (DD_STEP_LATE_GATHER if late_gather else 0)
                  | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
                  | (DD_STEP_PIPELINE if pipeline else 0)
-                 | (DD_STEP_CORRECT_MISSES if correct_misses else 0))
+                 | (DD_STEP_CORRECT_MISSES if correct_misses else 0)
+                 | (DD_STEP_LANDMARKS if landmarks else 0))
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 

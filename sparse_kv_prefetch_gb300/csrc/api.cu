@@ -115,6 +115,30 @@ WsLayout ws_layout(const Dims& d) {
   return w;
 }
 
+dd_status resolve_landmarks(const dd_shape* s, int chunk, LandmarkDims* out) {
+  Dims f;
+  dd_status st = resolve(s, &f);
+  if (st != DD_OK) return st;
+  if (chunk < 2 || f.span % chunk != 0 || f.k % chunk != 0) return DD_ERR_UNSUPPORTED;
+  if (f.d != 64 && f.d != 128) return DD_ERR_UNSUPPORTED;  // fp32 landmark rows <= 512 B
+  dd_shape ls = *s;
+  ls.ctx_len = f.span / chunk;
+  ls.top_k = f.k / chunk;
+  ls.window = 0;
+  ls.dtype = DD_F32;
+  LandmarkDims L;
+  st = resolve(&ls, &L.lm);
+  if (st != DD_OK) return st;
+  L.full = f;
+  L.chunk = chunk;
+  L.lay = ws_layout(L.lm);
+  L.q32 = L.lay.total;
+  L.chunks = L.q32 + align256((size_t)f.B * f.Hq * f.d * sizeof(float));
+  L.total = L.chunks + align256((size_t)f.U * L.lm.k * sizeof(int32_t));
+  *out = L;
+  return DD_OK;
+}
+
 }  // namespace dd
 
 using namespace dd;
@@ -357,6 +381,77 @@ dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_
                                   vh, k_buf_out, v_buf_out, miss_out, mass_out, s));
 }
 
+dd_status dd_landmarks_size(const dd_shape* shape, int chunk, size_t* bytes) {
+  if (!bytes) return DD_ERR_INVALID_ARG;
+  LandmarkDims L;
+  dd_status st = resolve_landmarks(shape, chunk, &L);
+  if (st != DD_OK) return st;
+  *bytes = (size_t)L.full.U * L.lm.n * L.full.d * sizeof(float);
+  return DD_OK;
+}
+
+dd_status dd_landmarks_workspace_size(const dd_shape* shape, int chunk, size_t* bytes) {
+  if (!bytes) return DD_ERR_INVALID_ARG;
+  LandmarkDims L;
+  dd_status st = resolve_landmarks(shape, chunk, &L);
+  if (st != DD_OK) return st;
+  *bytes = L.total;
+  return DD_OK;
+}
+
+dd_status dd_build_landmarks(const dd_shape* shape, int chunk, const void* k_dev,
+                             float* landmarks_out, dd_stream_t stream) {
+  LandmarkDims L;
+  dd_status st = resolve_landmarks(shape, chunk, &L);
+  if (st != DD_OK) return st;
+  if (!k_dev || !landmarks_out) return DD_ERR_INVALID_ARG;
+  if (!aligned16(k_dev) || !aligned16(landmarks_out)) return DD_ERR_INVALID_ARG;
+  if (!all_device({k_dev, landmarks_out})) return DD_ERR_INVALID_ARG;
+  return cuda_status(
+      launch_landmarks(L.full, chunk, k_dev, landmarks_out, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+namespace {
+// Landmark selection into `rows` (the k expanded rows) and `sel` (chunk scores).
+cudaError_t landmark_select(const LandmarkDims& L, const void* q, const void* landmarks,
+                            int32_t* rows, float* sel, float* lse, char* ws, cudaStream_t st) {
+  const Dims& f = L.full;
+  const float* q32 = static_cast<const float*>(q);
+  if (f.dtype == DD_BF16) {
+    float* tmp = reinterpret_cast<float*>(ws + L.q32);
+    cudaError_t e = launch_to_f32(q, tmp, f.B * f.Hq * f.d, st);
+    if (e != cudaSuccess) return e;
+    q32 = tmp;
+  }
+  float* logits = reinterpret_cast<float*>(ws + L.lay.logits);
+  float2* part = reinterpret_cast<float2*>(ws + L.lay.part);
+  int32_t* chunks = reinterpret_cast<int32_t*>(ws + L.chunks);
+  cudaError_t e = launch_score(L.lm, q32, landmarks, logits, part, st);
+  if (e == cudaSuccess) e = launch_topk(L.lm, logits, part, chunks, sel, lse, st);
+  if (e == cudaSuccess) e = launch_expand(chunks, rows, f.U, L.lm.k, L.chunk, st);
+  return e;
+}
+}  // namespace
+
+dd_status dd_score_topk_landmarks(const dd_shape* shape, int chunk, const void* q_spec,
+                                  const float* landmarks, int32_t* idx_out, float* chunk_score_out,
+                                  float* lse_out, void* workspace, size_t ws_bytes,
+                                  dd_stream_t stream) {
+  LandmarkDims L;
+  dd_status st = resolve_landmarks(shape, chunk, &L);
+  if (st != DD_OK) return st;
+  if (!q_spec || !landmarks || !idx_out || !chunk_score_out || !workspace)
+    return DD_ERR_INVALID_ARG;
+  if (!aligned16(q_spec) || !aligned16(landmarks) || !aligned16(workspace))
+    return DD_ERR_INVALID_ARG;
+  if (ws_bytes < L.total) return DD_ERR_INVALID_ARG;
+  if (!all_device({q_spec, landmarks, idx_out, chunk_score_out, lse_out, workspace}))
+    return DD_ERR_INVALID_ARG;
+  return cuda_status(landmark_select(L, q_spec, landmarks, idx_out, chunk_score_out, lse_out,
+                                     static_cast<char*>(workspace),
+                                     reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"
 
 // ------------------------------------------------------------------ context
@@ -392,6 +487,11 @@ struct dd_ctx {
   int corr_layers;
   int last_corr_layers;
   cudaEvent_t ev_done;
+  // Landmark selection (DD_STEP_LANDMARKS), set by dd_ctx_set_landmark_chunk.
+  int lm_chunk;
+  LandmarkDims lm;
+  void* lm_ws;  // its own workspace: under DD_STEP_PIPELINE the selection of
+                // layer l+1 runs beside the attention of layer l
 };
 
 namespace {
@@ -417,6 +517,7 @@ void ctx_free(dd_ctx* c) {
   cudaFree(c->vb_true);
   cudaFree(c->miss);
   cudaFree(c->mass);
+  cudaFree(c->lm_ws);
   if (c->ev_done) cudaEventDestroy(c->ev_done);
   if (c->ev_join) cudaEventDestroy(c->ev_join);
   for (cudaEvent_t e : c->tev) cudaEventDestroy(e);
@@ -522,6 +623,34 @@ void dd_ctx_destroy(dd_ctx* ctx) { ctx_free(ctx); }
 
 size_t dd_ctx_device_bytes(const dd_ctx* ctx) { return ctx ? ctx->device_bytes : 0; }
 
+dd_status dd_ctx_set_landmark_chunk(dd_ctx* c, int chunk) {
+  if (!c) return DD_ERR_INVALID_ARG;
+  LandmarkDims L;
+  dd_status st = resolve_landmarks(&c->shape, chunk, &L);
+  if (st != DD_OK) return st;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device) return DD_ERR_INVALID_ARG;
+  const size_t have = c->lm_chunk ? c->lm.total : 0;
+  if (L.total > have) {
+    cudaDeviceSynchronize();  // a step may still use the old buffer
+    cudaFree(c->lm_ws);
+    c->device_bytes -= have;
+    c->lm_ws = nullptr;
+    c->lm_chunk = 0;
+    if (cudaMalloc(&c->lm_ws, L.total) != cudaSuccess) {
+      c->lm_ws = nullptr;
+      cudaGetLastError();
+      return DD_ERR_OOM;
+    }
+    c->device_bytes += L.total;
+  } else {
+    L.total = have;  // keep the larger buffer's size on record
+  }
+  c->lm = L;
+  c->lm_chunk = chunk;
+  return DD_OK;
+}
+
 dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
                          dd_stream_t compute, dd_stream_t copy, int flags) {
   if (!c || !layers || n_layers < 1) return DD_ERR_INVALID_ARG;
@@ -545,6 +674,14 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   const bool timing = (flags & DD_STEP_TIMING) != 0;
   const int gather_mode = (flags & DD_STEP_GATHER_LSU) ? 1 : 0;
   const bool correct = (flags & DD_STEP_CORRECT_MISSES) != 0;
+  const bool use_lm = (flags & DD_STEP_LANDMARKS) != 0;
+  if (use_lm) {
+    if (c->lm_chunk == 0 || correct) return DD_ERR_UNSUPPORTED;
+    for (int l = 0; l < n_layers; ++l) {
+      if (!layers[l].landmarks || !aligned16(layers[l].landmarks)) return DD_ERR_INVALID_ARG;
+      if (!all_device({layers[l].landmarks})) return DD_ERR_INVALID_ARG;
+    }
+  }
   if (correct) {
     if (d.k > kMaxCorrectK) return DD_ERR_UNSUPPORTED;
     if ((flags & DD_STEP_PIPELINE) && copy && copy != compute) return DD_ERR_UNSUPPORTED;
@@ -575,6 +712,16 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   auto score_topk = [&](int l) -> cudaError_t {
     const int s = l & 1;
     if (timing) cudaEventRecord(T(l, PH_SCORE0), C);
+    if (use_lm) {
+      // Landmark selection: phase "score" covers it all, "top-k" is empty.
+      cudaError_t e = landmark_select(c->lm, layers[l].q_spec, layers[l].landmarks, c->idx[s],
+                                      c->sel[s], c->lse, static_cast<char*>(c->lm_ws), C);
+      if (e != cudaSuccess) return e;
+      if (timing) cudaEventRecord(T(l, PH_SCORE1), C);
+      if (timing) cudaEventRecord(T(l, PH_TOPK1), C);
+      launches += (d.dtype == DD_BF16 ? 1 : 0) + kScoreLaunches + kTopkLaunches + 1;
+      return cudaEventRecord(c->ev_idx[s], C);
+    }
     cudaError_t e = launch_score(d, layers[l].q_spec, layers[l].k_dev, logits, part, C);
     if (e != cudaSuccess) return e;
     if (timing) cudaEventRecord(T(l, PH_SCORE1), C);

@@ -52,6 +52,25 @@ cudaError_t launch_fixup(const Dims& d, const int32_t* idx_spec, const int32_t* 
                          const void* k_host, const void* v_host, void* kb_out, void* vb_out,
                          int32_t* miss_out, float* mass_out, cudaStream_t st);
 
+// Landmark selection (landmark.cu).
+cudaError_t launch_landmarks(const Dims& d, int chunk, const void* k_dev, float* landmarks,
+                             cudaStream_t st);
+cudaError_t launch_expand(const int32_t* chunks, int32_t* rows, int units, int kc, int chunk,
+                          cudaStream_t st);
+cudaError_t launch_to_f32(const void* x_bf16, float* y, int count, cudaStream_t st);
+
+// Shapes of landmark selection: `full` is the layer, `lm` the landmark "key
+// cache" (M = (n - W) / chunk rows of fp32, k / chunk to select, no window).
+// Workspace offsets of the fp32 queries and the selected chunk ids follow
+// lm's own layout.
+struct LandmarkDims {
+  Dims full, lm;
+  WsLayout lay;
+  size_t q32, chunks, total;
+  int chunk;
+};
+dd_status resolve_landmarks(const dd_shape* s, int chunk, LandmarkDims* out);
+
 // Number of kernels each launcher enqueues.
 constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 2, kAttnLaunches = 2,
               kFixupLaunches = 1;

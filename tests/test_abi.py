@@ -91,6 +91,39 @@ def test_null_and_misaligned_pointers_rejected():
     assert lib.dd_decode_step(None, None, 0, None, None, 0) == dd.DD_ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("kw,chunk,status", [
+    (dict(), 1, dd.DD_ERR_UNSUPPORTED),                 # a chunk of one row is not a chunk
+    (dict(), 0, dd.DD_ERR_UNSUPPORTED),
+    (dict(), 32, dd.DD_ERR_UNSUPPORTED),                # 32 divides k = 64, not n - W = 4080
+    (dict(), 17, dd.DD_ERR_UNSUPPORTED),                # 17 divides n - W = 4080, not k = 64
+    (dict(head_dim=256), 16, dd.DD_ERR_UNSUPPORTED),    # landmarks: d in {64, 128}
+    (dict(window=4096), 16, dd.DD_ERR_INVALID_ARG),     # the shape itself is invalid
+])
+def test_bad_landmark_chunks_rejected(kw, chunk, status):
+    n = ctypes.c_size_t()
+    st = dd.lib().dd_landmarks_size(ctypes.byref(_shape(**kw).c()), chunk, ctypes.byref(n))
+    assert st == status
+
+
+def test_landmark_sizes():
+    shp = _shape()  # n - W = 4080 = 255 * 16, k = 64 = 4 * 16
+    M = 4080 // 16
+    assert dd.landmarks_size(shp, 16) == 2 * 2 * M * 128 * 4
+    ws = dd.landmarks_workspace_size(shp, 16)
+    assert ws % 256 == 0
+    assert ws >= 2 * 8 * M * 4 + 2 * 8 * 128 * 4 + 2 * 2 * 4 * 4  # logits, fp32 q, chunk ids
+    assert ws < dd.workspace_size(shp)  # M = (n - W) / c logits instead of n
+    lib = dd.lib()
+    c = shp.c()
+    assert lib.dd_build_landmarks(ctypes.byref(c), 16, None, 16, None) == dd.DD_ERR_INVALID_ARG
+    assert lib.dd_build_landmarks(ctypes.byref(c), 16, 16, 8, None) == dd.DD_ERR_INVALID_ARG
+    st = lib.dd_score_topk_landmarks(ctypes.byref(c), 16, 16, 16, 16, 16, None, 16, 1024, None)
+    assert st == dd.DD_ERR_INVALID_ARG  # workspace too small
+    st = lib.dd_score_topk_landmarks(ctypes.byref(c), 16, 16, 16, None, 16, None, 16, ws, None)
+    assert st == dd.DD_ERR_INVALID_ARG  # no index output
+    assert lib.dd_ctx_set_landmark_chunk(None, 16) == dd.DD_ERR_INVALID_ARG
+
+
 def test_pageable_host_store_rejected_by_binding():
     import torch
     shp = _shape()
