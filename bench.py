@@ -313,10 +313,6 @@ def run_ours(args, rank, world):
         for s_ in range(D):
             dd.build_landmarks(shape, C, K_d[s_], lm_d[s_])
         ctx.set_landmark_chunk(C)
-    layers = dd.Ctx.pack([dd.LayerIO(qs_d[l % D], q_d[l % D], K_d[l % D], K_h[l % D],
-                                     V_h[l % D], vwin_d[l % D] if W > 0 else None, outs[l],
-                                     lm_d[l % D] if C else None)
-                          for l in range(L)])
     torch.cuda.synchronize()
 
     # Host-link probe: one large contiguous pinned H2D copy, median of 10.
@@ -383,6 +379,22 @@ def run_ours(args, rank, world):
             compute.synchronize()
             pred_miss.append(c_miss.cpu().numpy().copy())
             pred_mass.append(c_mass.cpu().numpy().copy())
+        # Recall as a function of the speculation noise: q = q_spec + sigma N(0, 1)
+        # (seeded, rounded to the stored dtype), on the first two layer slots.
+        pred_sigma = {}
+        gen = torch.Generator(device=dev)
+        for sigma in (0.0, 0.05, 0.1, 0.2, 0.4, 0.8):
+            gen.manual_seed(4321)
+            miss = []
+            for s_ in range(min(D, 2)):
+                q_sig = (qs_d[s_].float() + sigma * torch.randn(
+                    qs_d[s_].shape, generator=gen, device=dev)).to(dt)
+                dd.gather_h2d(shape, K_h[s_], V_h[s_], g_idx[s_], g_kb, g_vb, stream=compute)
+                dd.correct_misses(shape, q_sig, K_d[s_], g_idx[s_], g_kb, g_vb, K_h[s_], V_h[s_],
+                                  c_idx, c_kb, c_vb, c_miss, c_mass, g_ws, stream=compute)
+                compute.synchronize()
+                miss.append(c_miss.cpu().numpy().copy())
+            pred_sigma[str(sigma)] = float(1.0 - np.mean(miss) / k)
         del c_kb, c_vb
     predictability = None
     if pred_miss:
@@ -395,19 +407,56 @@ def run_ours(args, rank, world):
                      "|chunk rows selected with q_spec & TopK(q)| / k")
                     + " and the real query's selection score captured by the prefetched rows,"
                       " over all layer slots and units",
+            "recall_vs_sigma": pred_sigma,
+            "recall_vs_sigma_what": "q = q_spec + sigma N(0,1) drawn on the device, layer "
+                                    "slots 0-1, all units",
         }
     del g_ws, g_kb, g_vb
+
+    # Device residency of the step.  With landmarks the key cache itself is
+    # not needed: the selection reads the landmarks and the attention reads
+    # the window's keys from their own buffer.
+    kwin_d = None
+    if C:
+        kwin_d = K_d[:, :, :, n - W:, :].contiguous() if W > 0 else None
+        K_d = None  # frees the key cache
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        resident = lm_d.numel() * 4 + (2 * kwin_d.numel() * kwin_d.element_size() if W else 0)
+    else:
+        resident = K_d.numel() * K_d.element_size() + (
+            vwin_d.numel() * vwin_d.element_size() if W else 0)
+
+    def layer_io(l, qs, q):
+        if C:
+            return dd.LayerIO(qs, q, None, K_h[l % D], V_h[l % D],
+                              vwin_d[l % D] if W > 0 else None, outs[l], lm_d[l % D],
+                              kwin_d[l % D] if W > 0 else None)
+        return dd.LayerIO(qs, q, K_d[l % D], K_h[l % D], V_h[l % D],
+                          vwin_d[l % D] if W > 0 else None, outs[l])
+
+    layers = dd.Ctx.pack([layer_io(l, qs_d[l % D], q_d[l % D]) for l in range(L)])
 
     def step(copy_stream, timing=True):
         ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
                         late_gather=late, pipeline=pipe, gather_mode=args.gather_mode,
                         correct_misses=args.correct_misses, landmarks=bool(C))
-        return ctx.timings() if timing else None
+
+    def recorded(n_steps):
+        """Phase times and per-layer scoring times of the last n timed steps,
+        read after they ran (the events of every step stay in the context's
+        ring, so the timed steps are enqueued back to back)."""
+        ts = [ctx.timings(back=i) for i in reversed(range(n_steps))]
+        sc = [x for i in reversed(range(n_steps)) for x in ctx.score_times(L, back=i)]
+        return ts, sc
 
     compute.wait_stream(torch.cuda.current_stream())
     for _ in range(max(3, args.warmup)):
         step(copy)
     torch.cuda.synchronize()
+    n_serial = max(3, args.steps // 4)
+    n_phase = max(3, args.steps // 2)
+    ctx.set_timing_depth(max(args.steps, n_serial, n_phase))
 
     # Timed region: K overlapped steps, device time on the compute stream.
     clocks = ClockSampler(dev.index)
@@ -416,23 +465,29 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(compute)
-    phases, score_ms, launches = [], [], 0
     for _ in range(args.steps):
-        t = step(copy)
-        phases.append(t)
-        score_ms.extend(ctx.score_times(L))
-        launches += t["launches"]
+        step(copy, timing="light")  # events around the scoring phase only
     ev1.record(compute)
     torch.cuda.synchronize()
     barrier(world)
     clk = clocks.stop()
+    timed, score_ms = recorded(args.steps)
+    launches = sum(t["launches"] for t in timed)
+
+    # Phase breakdown: the same steps with events around every phase.
+    for _ in range(n_phase):
+        step(copy)
+    torch.cuda.synchronize()
+    phases, _ = recorded(n_phase)
     total_s = ev0.elapsed_time(ev1) * 1e-3
     total_s = max_over_ranks(total_s, world)
     value = job_throughput(L, args.steps, total_s, world)
 
     # Serial schedule (same work, one stream) for the hidden fraction.
-    serial = [step(None) for _ in range(max(3, args.steps // 4))]
+    for _ in range(n_serial):
+        step(None)
     torch.cuda.synchronize()
+    serial, _ = recorded(n_serial)
 
     # End to end through the public API: per step copy every layer's q_spec and q
     # from pinned host memory, run the step, read every layer's output back.
@@ -441,10 +496,7 @@ def run_ours(args, rank, world):
     q_l = torch.empty((L, B, Hq, d), dtype=dt, device=dev)
     qs_src = torch.stack([qs_h[l % D] for l in range(L)]).pin_memory()
     q_src = torch.stack([q_h[l % D] for l in range(L)]).pin_memory()
-    layers_e2e = dd.Ctx.pack([dd.LayerIO(qs_l[l], q_l[l], K_d[l % D], K_h[l % D], V_h[l % D],
-                                         vwin_d[l % D] if W > 0 else None, outs[l],
-                                         lm_d[l % D] if C else None)
-                              for l in range(L)])
+    layers_e2e = dd.Ctx.pack([layer_io(l, qs_l[l], q_l[l]) for l in range(L)])
     e2e_steps = max(3, args.steps // 2)
 
     def e2e_step():
@@ -518,6 +570,7 @@ def run_ours(args, rank, world):
         "phase_ms_per_step": {kk: statistics.mean(p[kk] for p in phases)
                               for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms", "attn_ms")},
         "serial_step_ms": t_ser,
+        "timed_step_ms_median": statistics.median(p["step_ms"] for p in timed),
         "serial_phase_ms_per_step": {kk: statistics.mean(p[kk] for p in serial)
                                      for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms",
                                                 "attn_ms")},
@@ -542,6 +595,9 @@ def run_ours(args, rank, world):
         "host_store": {"bytes": store_bytes, "huge_page_bytes": dd.host_page_bytes(),
                        "huge_page_fraction": huge_frac},
         "ctx_device_bytes": ctx.device_bytes,
+        "hbm_resident_kv_bytes": resident,
+        "hbm_resident_kv_what": ("fp32 landmarks + window K and V of every layer slot" if C else
+                                 "key cache + window V of every layer slot"),
     }
     ctx.close()
     print(json.dumps(line), flush=True)

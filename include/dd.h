@@ -299,13 +299,17 @@ typedef struct dd_ctx dd_ctx;
 typedef struct {
   const void* q_spec; /* device [B][H_q][d] */
   const void* q;      /* device [B][H_q][d] */
-  const void* k_dev;  /* device [B][H_kv][n][d] */
+  const void* k_dev;  /* device [B][H_kv][n][d] (see k_win) */
   const void* k_host; /* pinned host [B][H_kv][n][d] */
   const void* v_host; /* pinned host [B][H_kv][n][d] */
   const void* v_win;  /* device [B][H_kv][W][d] (NULL if W = 0) */
   float* out;         /* device [B][H_q][d] */
   const float* landmarks; /* device [B][H_kv][(n-W)/c][d] fp32 from dd_build_landmarks;
                              read only under DD_STEP_LANDMARKS (else may be NULL) */
+  const void* k_win;  /* device [B][H_kv][W][d], the window's keys, or NULL: then
+                         they are read from k_dev.  Under DD_STEP_LANDMARKS with
+                         k_win (or W = 0) k_dev may be NULL: nothing of size n
+                         then stays on the device */
 } dd_layer_io;
 
 /*
@@ -337,6 +341,10 @@ enum {
                               attention of each layer on `copy`, as soon as its
                               indices are ready (compute runs at most two layers
                               ahead); attention never runs beside a gather */
+  DD_STEP_TIMING_LIGHT = 64, /* like DD_STEP_TIMING, but only the step's first
+                              and last events and those around each layer's
+                              scoring (selection) phase; dd_ctx_timings then
+                              reports step_ms and score_ms only */
   DD_STEP_LANDMARKS = 32   /* select with dd_score_topk_landmarks over each
                               layer's `landmarks` instead of scoring every key
                               (chunk set by dd_ctx_set_landmark_chunk; not
@@ -378,6 +386,19 @@ typedef struct {
 dd_status dd_ctx_timings(dd_ctx* ctx, dd_phase_times* out);
 
 /*
+ * Keep the events of the last `depth` timed steps (1 <= depth <= 4096;
+ * default 1), so that several timed steps can be enqueued back to back and
+ * read afterwards.  Forgets the steps recorded so far.  Must not be called
+ * while a timed step is being enqueued on another thread.
+ */
+dd_status dd_ctx_set_timing_depth(dd_ctx* ctx, int depth);
+
+/* Phase times of the timed step `back` steps before the last one (0: the
+ * last); waits for that step.  DD_ERR_INVALID_ARG if the ring no longer holds
+ * it. */
+dd_status dd_ctx_step_timings(dd_ctx* ctx, int back, dd_phase_times* out);
+
+/*
  * Miss statistics of the last step run with DD_STEP_CORRECT_MISSES, for its
  * first n_layers layers (waits for that step): misses [n_layers][B*H_kv]
  * (rows of the real query's top-k that the prediction had not fetched) and
@@ -386,8 +407,11 @@ dd_status dd_ctx_timings(dd_ctx* ctx, dd_phase_times* out);
  */
 dd_status dd_ctx_correction_stats(dd_ctx* ctx, int32_t* misses, float* mass, int n_layers);
 
-/* Per-layer scoring-kernel times (ms) of the last timed step; n entries max. */
+/* Per-layer scoring-kernel times (ms) of the last timed step; n entries max.
+ * Under DD_STEP_LANDMARKS the time covers the whole landmark selection. */
 dd_status dd_ctx_score_times(dd_ctx* ctx, float* out_ms, int n);
+/* The same for the timed step `back` steps before the last one. */
+dd_status dd_ctx_step_score_times(dd_ctx* ctx, int back, float* out_ms, int n);
 
 #ifdef __cplusplus
 }

@@ -28,6 +28,7 @@ DD_STEP_GATHER_LSU = 4
 DD_STEP_PIPELINE = 8
 DD_STEP_CORRECT_MISSES = 16
 DD_STEP_LANDMARKS = 32
+DD_STEP_TIMING_LIGHT = 64
 
 
 class DDError(RuntimeError):
@@ -45,7 +46,7 @@ class dd_layer_io(ctypes.Structure):
     _fields_ = [("q_spec", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k_dev", ctypes.c_void_p),
                 ("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p),
                 ("v_win", ctypes.c_void_p), ("out", ctypes.c_void_p),
-                ("landmarks", ctypes.c_void_p)]
+                ("landmarks", ctypes.c_void_p), ("k_win", ctypes.c_void_p)]
 
 
 class dd_phase_times(ctypes.Structure):
@@ -114,6 +115,11 @@ def _lib():
             "dd_score_topk_landmarks": ([S, ctypes.c_int, P, P, P, P, P, P, ctypes.c_size_t, P],
                                         ctypes.c_int),
             "dd_ctx_set_landmark_chunk": ([P, ctypes.c_int], ctypes.c_int),
+            "dd_ctx_set_timing_depth": ([P, ctypes.c_int], ctypes.c_int),
+            "dd_ctx_step_timings": ([P, ctypes.c_int, ctypes.POINTER(dd_phase_times)],
+                                    ctypes.c_int),
+            "dd_ctx_step_score_times": ([P, ctypes.c_int, ctypes.POINTER(ctypes.c_float),
+                                         ctypes.c_int], ctypes.c_int),
         }
         for name, (args, res) in sig.items():
             f = getattr(L, name)
@@ -298,6 +304,7 @@ class LayerIO(NamedTuple):
     v_win: object
     out: object
     landmarks: object = None
+    k_win: object = None
 
 
 class Ctx:
@@ -332,21 +339,23 @@ class Ctx:
         for i, io in enumerate(layers):
             arr[i] = dd_layer_io(_dev(io.q_spec), _dev(io.q), _dev(io.k_dev), _host(io.k_host),
                                  _host(io.v_host), _dev(io.v_win), _dev(io.out),
-                                 _dev(io.landmarks))
+                                 _dev(io.landmarks), _dev(io.k_win))
         return arr
 
     def set_landmark_chunk(self, chunk: int):
         """Chunk size of landmark selection (decode_step(landmarks=True))."""
         _check(_lib().dd_ctx_set_landmark_chunk(self._h, chunk), "dd_ctx_set_landmark_chunk")
 
-    def decode_step(self, layers, compute=None, copy=None, timing: bool = False,
+    def decode_step(self, layers, compute=None, copy=None, timing=False,
                     late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False,
                     correct_misses: bool = False, landmarks: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
-        flags = ((DD_STEP_TIMING if timing else 0) | (DD_STEP_LATE_GATHER if late_gather else 0)
+        # timing: False, True (every phase) or "light" (step and scoring only)
+        flags = ((DD_STEP_TIMING_LIGHT if timing == "light" else DD_STEP_TIMING if timing else 0)
+                 | (DD_STEP_LATE_GATHER if late_gather else 0)
                  | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
                  | (DD_STEP_PIPELINE if pipeline else 0)
                  | (DD_STEP_CORRECT_MISSES if correct_misses else 0)
@@ -354,9 +363,14 @@ class Ctx:
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 
-    def timings(self) -> dict:
+    def set_timing_depth(self, depth: int):
+        """Keep the events of the last `depth` timed steps (read with back=...)."""
+        _check(_lib().dd_ctx_set_timing_depth(self._h, depth), "dd_ctx_set_timing_depth")
+
+    def timings(self, back: int = 0) -> dict:
+        """Phase times of the timed step `back` steps before the last one."""
         t = dd_phase_times()
-        _check(_lib().dd_ctx_timings(self._h, ctypes.byref(t)), "dd_ctx_timings")
+        _check(_lib().dd_ctx_step_timings(self._h, back, ctypes.byref(t)), "dd_ctx_step_timings")
         return {f: getattr(t, f) for f, _ in dd_phase_times._fields_}
 
     def correction_stats(self, n_layers: int):
@@ -370,7 +384,7 @@ class Ctx:
                                               n_layers), "dd_ctx_correction_stats")
         return misses, mass
 
-    def score_times(self, n: int):
+    def score_times(self, n: int, back: int = 0):
         buf = (ctypes.c_float * n)()
-        _check(_lib().dd_ctx_score_times(self._h, buf, n), "dd_ctx_score_times")
+        _check(_lib().dd_ctx_step_score_times(self._h, back, buf, n), "dd_ctx_step_score_times")
         return list(buf)

@@ -55,9 +55,10 @@ dd_status resolve(const dd_shape* s, Dims* o) {
   if (s->dtype != DD_F32 && s->dtype != DD_BF16) return DD_ERR_UNSUPPORTED;
   const int G = s->n_q_heads / s->n_kv_heads;
   if (G != 1 && G != 2 && G != 4 && G != 8) return DD_ERR_UNSUPPORTED;
-  const int chunk = score_chunk(s->dtype, s->head_dim);
-  if (chunk == 0) return DD_ERR_UNSUPPORTED;
   if (s->ctx_len > (1 << 30)) return DD_ERR_UNSUPPORTED;
+  const int chunk =
+      score_chunk(s->dtype, s->head_dim, (long long)s->batch * s->n_kv_heads, s->ctx_len);
+  if (chunk == 0) return DD_ERR_UNSUPPORTED;
   Dims d;
   d.B = s->batch;
   d.Hq = s->n_q_heads;
@@ -337,7 +338,7 @@ dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void
   if (ws_bytes < w.total) return DD_ERR_INVALID_ARG;
   if (!all_device({q, k_buf, v_buf, k_dev, v_win, out, workspace})) return DD_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace);
-  return cuda_status(launch_attn(d, q, k_buf, v_buf, k_dev, v_win, out,
+  return cuda_status(launch_attn(d, q, k_buf, v_buf, window_in_cache(k_dev, d), v_win, out,
                                  reinterpret_cast<float*>(ws + w.attn_o),
                                  reinterpret_cast<float2*>(ws + w.attn_ml),
                                  reinterpret_cast<cudaStream_t>(stream)));
@@ -456,7 +457,25 @@ dd_status dd_score_topk_landmarks(const dd_shape* shape, int chunk, const void* 
 
 // ------------------------------------------------------------------ context
 
+constexpr int kMaxTimingDepth = 4096;
+
 enum Phase { PH_SCORE0, PH_SCORE1, PH_TOPK1, PH_GATHER0, PH_GATHER1, PH_ATTN0, PH_ATTN1, PH_N };
+
+// The events of one timed step: PH_N per layer, plus the step's first and last.
+struct TimingSet {
+  std::vector<cudaEvent_t> tev;
+  cudaEvent_t t_begin = nullptr, t_end = nullptr;
+  int layers = 0;
+  int launches = 0;
+  bool light = false;  // DD_STEP_TIMING_LIGHT: only the scoring events
+  void release() {
+    for (cudaEvent_t e : tev) cudaEventDestroy(e);
+    tev.clear();
+    if (t_begin) cudaEventDestroy(t_begin);
+    if (t_end) cudaEventDestroy(t_end);
+    t_begin = t_end = nullptr;
+  }
+};
 
 struct dd_ctx {
   dd_shape shape;
@@ -472,11 +491,14 @@ struct dd_ctx {
   size_t device_bytes;
   cudaEvent_t ev_idx[2], ev_ready[2], ev_free[2], ev_join;
   // Timing: per layer PH_N events, plus the step's first and last.
-  std::vector<cudaEvent_t> tev;
-  cudaEvent_t t_begin, t_end;
-  int timed_layers;
-  int timed_launches;
-  bool timed_serial;
+  // A ring of t_depth event sets: timed step i records into set i % t_depth,
+  // so the last t_depth timed steps can be read without a host wait between
+  // steps.  t_last is the set of the last timed step, t_count how many timed
+  // steps the ring holds.
+  std::vector<TimingSet> tsets;
+  int t_depth;
+  int t_last;
+  int t_count;
   // Miss correction (DD_STEP_CORRECT_MISSES): the real query's indices and
   // rows, and per-layer statistics, grown to the largest layer count used.
   int32_t* idx_true;
@@ -520,9 +542,7 @@ void ctx_free(dd_ctx* c) {
   cudaFree(c->lm_ws);
   if (c->ev_done) cudaEventDestroy(c->ev_done);
   if (c->ev_join) cudaEventDestroy(c->ev_join);
-  for (cudaEvent_t e : c->tev) cudaEventDestroy(e);
-  if (c->t_begin) cudaEventDestroy(c->t_begin);
-  if (c->t_end) cudaEventDestroy(c->t_end);
+  for (TimingSet& t : c->tsets) t.release();
   if (prev >= 0) cudaSetDevice(prev);
   delete c;
 }
@@ -555,16 +575,24 @@ dd_status ensure_correction_buffers(dd_ctx* c, int n_layers) {
   return DD_OK;
 }
 
-dd_status ensure_timing_events(dd_ctx* c, int n_layers) {
+dd_status ensure_timing_events(TimingSet& t, int n_layers) {
   const size_t need = (size_t)n_layers * PH_N;
-  while (c->tev.size() < need) {
+  while (t.tev.size() < need) {
     cudaEvent_t e;
     if (cudaEventCreate(&e) != cudaSuccess) return DD_ERR_CUDA;
-    c->tev.push_back(e);
+    t.tev.push_back(e);
   }
-  if (!c->t_begin && cudaEventCreate(&c->t_begin) != cudaSuccess) return DD_ERR_CUDA;
-  if (!c->t_end && cudaEventCreate(&c->t_end) != cudaSuccess) return DD_ERR_CUDA;
+  if (!t.t_begin && cudaEventCreate(&t.t_begin) != cudaSuccess) return DD_ERR_CUDA;
+  if (!t.t_end && cudaEventCreate(&t.t_end) != cudaSuccess) return DD_ERR_CUDA;
   return DD_OK;
+}
+
+// The timing set of the timed step `back` steps before the last one.
+TimingSet* timing_set(dd_ctx* c, int back) {
+  if (back < 0 || back >= c->t_count) return nullptr;
+  TimingSet* t = &c->tsets[(size_t)((c->t_last - back + c->t_depth) % c->t_depth)];
+  if (cudaEventSynchronize(t->t_end) != cudaSuccess) return nullptr;
+  return t;
 }
 
 }  // namespace
@@ -581,6 +609,10 @@ dd_status dd_ctx_create(const dd_shape* shape, dd_ctx** out) {
   if (!c) return DD_ERR_OOM;
   c->shape = *shape;
   c->dims = d;
+  c->tsets.resize(1);
+  c->t_depth = 1;
+  c->t_last = -1;
+  c->t_count = 0;
   c->ws_lay = ws_layout(d);
   if (cudaGetDevice(&c->device) != cudaSuccess) {
     delete c;
@@ -657,21 +689,27 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   const Dims& d = c->dims;
   // Synchronous checks of every layer before anything is enqueued.
   std::vector<const void*> kh(n_layers), vh(n_layers);
+  // Without DD_STEP_LANDMARKS the key cache is scored, so k_dev is required;
+  // with it, k_dev is needed only for the window's keys, if k_win is NULL.
+  const bool lm_flag = (flags & DD_STEP_LANDMARKS) != 0;
   for (int l = 0; l < n_layers; ++l) {
     const dd_layer_io& io = layers[l];
-    if (!io.q_spec || !io.q || !io.k_dev || !io.k_host || !io.v_host || !io.out)
-      return DD_ERR_INVALID_ARG;
+    if (!io.q_spec || !io.q || !io.k_host || !io.v_host || !io.out) return DD_ERR_INVALID_ARG;
+    if (!io.k_dev && !(lm_flag && (io.k_win || d.W == 0))) return DD_ERR_INVALID_ARG;
     if (d.W > 0 && !io.v_win) return DD_ERR_INVALID_ARG;
     if (!aligned16(io.q_spec) || !aligned16(io.q) || !aligned16(io.k_dev) ||
         !aligned16(io.k_host) || !aligned16(io.v_host) || !aligned16(io.out) ||
-        (io.v_win && !aligned16(io.v_win)))
+        !aligned16(io.v_win) || !aligned16(io.k_win))
       return DD_ERR_INVALID_ARG;
     kh[l] = host_to_device(io.k_host);
     vh[l] = host_to_device(io.v_host);
     if (!kh[l] || !vh[l]) return DD_ERR_INVALID_ARG;
-    if (!all_device({io.q_spec, io.q, io.k_dev, io.v_win, io.out})) return DD_ERR_INVALID_ARG;
+    if (!all_device({io.q_spec, io.q, io.k_dev, io.v_win, io.k_win, io.out}))
+      return DD_ERR_INVALID_ARG;
   }
-  const bool timing = (flags & DD_STEP_TIMING) != 0;
+  const bool light = (flags & DD_STEP_TIMING_LIGHT) != 0;
+  const bool timing = light || (flags & DD_STEP_TIMING) != 0;
+  const bool phases = timing && !light;  // the events of every phase
   const int gather_mode = (flags & DD_STEP_GATHER_LSU) ? 1 : 0;
   const bool correct = (flags & DD_STEP_CORRECT_MISSES) != 0;
   const bool use_lm = (flags & DD_STEP_LANDMARKS) != 0;
@@ -688,8 +726,12 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     dd_status st = ensure_correction_buffers(c, n_layers);
     if (st != DD_OK) return st;
   }
+  TimingSet* ts = nullptr;
+  int t_slot = 0;
   if (timing) {
-    dd_status st = ensure_timing_events(c, n_layers);
+    t_slot = (c->t_last + 1) % c->t_depth;
+    ts = &c->tsets[(size_t)t_slot];
+    dd_status st = ensure_timing_events(*ts, n_layers);
     if (st != DD_OK) return st;
   }
   cudaStream_t C = reinterpret_cast<cudaStream_t>(compute);
@@ -700,7 +742,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   float2* part = reinterpret_cast<float2*>(ws + c->ws_lay.part);
   float* attn_o = reinterpret_cast<float*>(ws + c->ws_lay.attn_o);
   float2* attn_ml = reinterpret_cast<float2*>(ws + c->ws_lay.attn_ml);
-  auto T = [&](int l, int ph) { return c->tev[(size_t)l * PH_N + ph]; };
+  auto T = [&](int l, int ph) { return ts->tev[(size_t)l * PH_N + ph]; };
   int launches = 0;
 #define DD_TRY(x)                                   \
   do {                                              \
@@ -718,7 +760,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
                                       c->sel[s], c->lse, static_cast<char*>(c->lm_ws), C);
       if (e != cudaSuccess) return e;
       if (timing) cudaEventRecord(T(l, PH_SCORE1), C);
-      if (timing) cudaEventRecord(T(l, PH_TOPK1), C);
+      if (phases) cudaEventRecord(T(l, PH_TOPK1), C);
       launches += (d.dtype == DD_BF16 ? 1 : 0) + kScoreLaunches + kTopkLaunches + 1;
       return cudaEventRecord(c->ev_idx[s], C);
     }
@@ -727,7 +769,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     if (timing) cudaEventRecord(T(l, PH_SCORE1), C);
     e = launch_topk(d, logits, part, c->idx[s], c->sel[s], c->lse, C);
     if (e != cudaSuccess) return e;
-    if (timing) cudaEventRecord(T(l, PH_TOPK1), C);
+    if (phases) cudaEventRecord(T(l, PH_TOPK1), C);
     launches += kScoreLaunches + kTopkLaunches;
     return cudaEventRecord(c->ev_idx[s], C);
   };
@@ -741,10 +783,10 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       e = cudaStreamWaitEvent(X, c->ev_free[s], 0);
       if (e != cudaSuccess) return e;
     }
-    if (timing) cudaEventRecord(T(l, PH_GATHER0), X);
+    if (phases) cudaEventRecord(T(l, PH_GATHER0), X);
     e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X);
     if (e != cudaSuccess) return e;
-    if (timing) cudaEventRecord(T(l, PH_GATHER1), X);
+    if (phases) cudaEventRecord(T(l, PH_GATHER1), X);
     launches += kGatherLaunches;
     return cudaEventRecord(c->ev_ready[s], X);
   };
@@ -760,7 +802,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       e = cudaStreamWaitEvent(C, c->ev_ready[s], 0);
       if (e != cudaSuccess) return e;
     }
-    if (timing) cudaEventRecord(T(l, PH_ATTN0), A);
+    if (phases) cudaEventRecord(T(l, PH_ATTN0), A);
     const void* kb = c->kbuf[s];
     const void* vb = c->vbuf[s];
     if (correct) {
@@ -777,15 +819,17 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       kb = c->kb_true;
       vb = c->vb_true;
     }
-    e = launch_attn(d, layers[l].q, kb, vb, layers[l].k_dev, layers[l].v_win, layers[l].out,
-                    attn_o, attn_ml, A);
+    const WindowK kw = layers[l].k_win ? window_buffer(layers[l].k_win, d)
+                                       : window_in_cache(layers[l].k_dev, d);
+    e = launch_attn(d, layers[l].q, kb, vb, kw, layers[l].v_win, layers[l].out, attn_o, attn_ml,
+                    A);
     if (e != cudaSuccess) return e;
-    if (timing) cudaEventRecord(T(l, PH_ATTN1), A);
+    if (phases) cudaEventRecord(T(l, PH_ATTN1), A);
     launches += kAttnLaunches;
     return cudaEventRecord(c->ev_free[s], A);
   };
 
-  if (timing) DD_TRY(cudaEventRecord(c->t_begin, C));
+  if (timing) DD_TRY(cudaEventRecord(ts->t_begin, C));
   if (serial) {
     for (int l = 0; l < n_layers; ++l) {
       DD_TRY(score_topk(l));
@@ -833,28 +877,31 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   DD_TRY(cudaEventRecord(c->ev_done, C));
   if (correct) c->last_corr_layers = n_layers;
   if (timing) {
-    DD_TRY(cudaEventRecord(c->t_end, C));
-    c->timed_layers = n_layers;
-    c->timed_launches = launches;
-    c->timed_serial = serial;
+    DD_TRY(cudaEventRecord(ts->t_end, C));
+    ts->layers = n_layers;
+    ts->launches = launches;
+    ts->light = light;
+    c->t_last = t_slot;
+    c->t_count = std::min(c->t_count + 1, c->t_depth);
   }
 #undef DD_TRY
   return DD_OK;
 }
 
-dd_status dd_ctx_timings(dd_ctx* c, dd_phase_times* out) {
+dd_status dd_ctx_step_timings(dd_ctx* c, int back, dd_phase_times* out) {
   if (!c || !out) return DD_ERR_INVALID_ARG;
-  if (c->timed_layers <= 0) return DD_ERR_INVALID_ARG;
-  if (cudaEventSynchronize(c->t_end) != cudaSuccess) return DD_ERR_CUDA;
+  TimingSet* t = timing_set(c, back);
+  if (!t) return DD_ERR_INVALID_ARG;
   memset(out, 0, sizeof(*out));
   float ms = 0.f;
-  if (cudaEventElapsedTime(&ms, c->t_begin, c->t_end) != cudaSuccess) return DD_ERR_CUDA;
+  if (cudaEventElapsedTime(&ms, t->t_begin, t->t_end) != cudaSuccess) return DD_ERR_CUDA;
   out->step_ms = ms;
-  for (int l = 0; l < c->timed_layers; ++l) {
-    const cudaEvent_t* e = &c->tev[(size_t)l * PH_N];
+  for (int l = 0; l < t->layers; ++l) {
+    const cudaEvent_t* e = &t->tev[(size_t)l * PH_N];
     float a = 0.f;
     if (cudaEventElapsedTime(&a, e[PH_SCORE0], e[PH_SCORE1]) != cudaSuccess) return DD_ERR_CUDA;
     out->score_ms += a;
+    if (t->light) continue;
     if (cudaEventElapsedTime(&a, e[PH_SCORE1], e[PH_TOPK1]) != cudaSuccess) return DD_ERR_CUDA;
     out->topk_ms += a;
     if (cudaEventElapsedTime(&a, e[PH_GATHER0], e[PH_GATHER1]) != cudaSuccess) return DD_ERR_CUDA;
@@ -862,8 +909,20 @@ dd_status dd_ctx_timings(dd_ctx* c, dd_phase_times* out) {
     if (cudaEventElapsedTime(&a, e[PH_ATTN0], e[PH_ATTN1]) != cudaSuccess) return DD_ERR_CUDA;
     out->attn_ms += a;
   }
-  out->n_layers = c->timed_layers;
-  out->launches = c->timed_launches;
+  out->n_layers = t->layers;
+  out->launches = t->launches;
+  return DD_OK;
+}
+
+dd_status dd_ctx_timings(dd_ctx* c, dd_phase_times* out) { return dd_ctx_step_timings(c, 0, out); }
+
+dd_status dd_ctx_set_timing_depth(dd_ctx* c, int depth) {
+  if (!c || depth < 1 || depth > kMaxTimingDepth) return DD_ERR_INVALID_ARG;
+  for (size_t i = (size_t)depth; i < c->tsets.size(); ++i) c->tsets[i].release();
+  c->tsets.resize((size_t)depth);
+  c->t_depth = depth;
+  c->t_last = -1;
+  c->t_count = 0;
   return DD_OK;
 }
 
@@ -881,16 +940,20 @@ dd_status dd_ctx_correction_stats(dd_ctx* c, int32_t* misses, float* mass, int n
   return DD_OK;
 }
 
-dd_status dd_ctx_score_times(dd_ctx* c, float* out_ms, int n) {
+dd_status dd_ctx_step_score_times(dd_ctx* c, int back, float* out_ms, int n) {
   if (!c || !out_ms || n < 0) return DD_ERR_INVALID_ARG;
-  if (c->timed_layers <= 0) return DD_ERR_INVALID_ARG;
-  if (cudaEventSynchronize(c->t_end) != cudaSuccess) return DD_ERR_CUDA;
-  for (int l = 0; l < c->timed_layers && l < n; ++l) {
-    const cudaEvent_t* e = &c->tev[(size_t)l * PH_N];
+  TimingSet* t = timing_set(c, back);
+  if (!t) return DD_ERR_INVALID_ARG;
+  for (int l = 0; l < t->layers && l < n; ++l) {
+    const cudaEvent_t* e = &t->tev[(size_t)l * PH_N];
     if (cudaEventElapsedTime(&out_ms[l], e[PH_SCORE0], e[PH_SCORE1]) != cudaSuccess)
       return DD_ERR_CUDA;
   }
   return DD_OK;
+}
+
+dd_status dd_ctx_score_times(dd_ctx* c, float* out_ms, int n) {
+  return dd_ctx_step_score_times(c, 0, out_ms, n);
 }
 
 }  // extern "C"

@@ -34,10 +34,10 @@ struct AttnGeom {
 template <typename T, int D, int G>
 __global__ void __launch_bounds__(kAttnThreads)
     attn_partial_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k_buf,
-                        const uint4* __restrict__ v_buf, const uint4* __restrict__ k_dev,
+                        const uint4* __restrict__ v_buf, const uint4* __restrict__ k_win,
                         const uint4* __restrict__ v_win, float* __restrict__ part_o,
-                        float2* __restrict__ part_ml, int n, int k, int W, int Hq, int Hkv,
-                        int nsplit, float scale) {
+                        float2* __restrict__ part_ml, int kw_stride, int kw_off, int k, int W,
+                        int Hq, int Hkv, int nsplit, float scale) {
   using Geo = AttnGeom<T, D>;
   constexpr int VEC = Geo::kVec, LPR = Geo::kLpr, RPW = Geo::kRpw, NG = Geo::kGroups;
   constexpr int IT = Geo::kIt, V16 = LPR;
@@ -57,10 +57,12 @@ __global__ void __launch_bounds__(kAttnThreads)
   for (int g = 0; g < G; ++g) unpack(ld_ro(q + (size_t)(b * Hq + hk * G + g) * V16 + sub), qf[g]);
 
   // Row r of the unit's attended set: gathered row r (r < k) or window row
-  // r - k, i.e. cached position n - W + (r - k).
+  // r - k, i.e. cached position n - W + (r - k): row kw_off + (r - k) of the
+  // unit's kw_stride rows of k_win (the key cache: stride n, offset n - W; a
+  // window buffer: stride W, offset 0).
   auto k_row = [&](int r) -> const uint4* {
     return (r < k) ? k_buf + ((size_t)u * k + r) * V16
-                   : k_dev + ((size_t)u * n + (n - W + (r - k))) * V16;
+                   : k_win + ((size_t)u * kw_stride + kw_off + (r - k)) * V16;
   };
   auto v_row = [&](int r) -> const uint4* {
     return (r < k) ? v_buf + ((size_t)u * k + r) * V16 : v_win + ((size_t)u * W + (r - k)) * V16;
@@ -182,7 +184,7 @@ __global__ void attn_merge_kernel(const float* __restrict__ part_o,
 
 template <typename T, int D, int G>
 cudaError_t launch_typed(const Dims& d, const void* q, const void* kb, const void* vb,
-                         const void* kd, const void* vw, float* out, float* po, float2* pml,
+                         const WindowK& kw, const void* vw, float* out, float* po, float2* pml,
                          cudaStream_t st) {
   static unsigned long long prepared = 0, prepared_merge = 0;
   cudaError_t e0 = prepare_kernel(attn_partial_kernel<T, D, G>, &prepared, 0);
@@ -192,8 +194,8 @@ cudaError_t launch_typed(const Dims& d, const void* q, const void* kb, const voi
   const dim3 grid((unsigned)d.U, (unsigned)d.nsplit);
   attn_partial_kernel<T, D, G><<<grid, kAttnThreads, 0, st>>>(
       static_cast<const uint4*>(q), static_cast<const uint4*>(kb), static_cast<const uint4*>(vb),
-      static_cast<const uint4*>(kd), static_cast<const uint4*>(vw), po, pml, d.n, d.k, d.W, d.Hq,
-      d.Hkv, d.nsplit, scale);
+      static_cast<const uint4*>(kw.p), static_cast<const uint4*>(vw), po, pml, kw.stride, kw.off,
+      d.k, d.W, d.Hq, d.Hkv, d.nsplit, scale);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_merge_kernel<<<(unsigned)(d.B * d.Hq), D, 0, st>>>(po, pml, out, d.nsplit, D);
@@ -201,8 +203,9 @@ cudaError_t launch_typed(const Dims& d, const void* q, const void* kb, const voi
 }
 
 template <typename T, int D>
-cudaError_t launch_g(const Dims& d, const void* q, const void* kb, const void* vb, const void* kd,
-                     const void* vw, float* out, float* po, float2* pml, cudaStream_t st) {
+cudaError_t launch_g(const Dims& d, const void* q, const void* kb, const void* vb,
+                     const WindowK& kd, const void* vw, float* out, float* po, float2* pml,
+                     cudaStream_t st) {
   switch (d.G) {
     case 1: return launch_typed<T, D, 1>(d, q, kb, vb, kd, vw, out, po, pml, st);
     case 2: return launch_typed<T, D, 2>(d, q, kb, vb, kd, vw, out, po, pml, st);
@@ -215,7 +218,7 @@ cudaError_t launch_g(const Dims& d, const void* q, const void* kb, const void* v
 }  // namespace
 
 cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const void* v_buf,
-                        const void* k_dev, const void* v_win, float* out, float* part_o,
+                        const WindowK& k_dev, const void* v_win, float* out, float* part_o,
                         float2* part_ml, cudaStream_t st) {
   if (d.dtype == DD_BF16) {
     if (d.d == 64) return launch_g<bf16_t, 64>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, st);

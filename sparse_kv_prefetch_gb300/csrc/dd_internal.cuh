@@ -40,8 +40,20 @@ cudaError_t launch_topk(const Dims& d, const float* logits, const float2* part, 
 cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
                           const int32_t* idx, void* k_buf, void* v_buf, int mode,
                           cudaStream_t st);
+// Where the attention reads the window's keys: row off + i (i < W) of each
+// unit's `stride` rows starting at p.
+struct WindowK {
+  const void* p;
+  int stride, off;
+};
+// The window inside the key cache [U][n][d], or a window buffer [U][W][d].
+inline WindowK window_in_cache(const void* k_dev, const Dims& d) {
+  return WindowK{k_dev, d.n, d.n - d.W};
+}
+inline WindowK window_buffer(const void* k_win, const Dims& d) { return WindowK{k_win, d.W, 0}; }
+
 cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const void* v_buf,
-                        const void* k_dev, const void* v_win, float* out, float* part_o,
+                        const WindowK& k_win, const void* v_win, float* out, float* part_o,
                         float2* part_ml, cudaStream_t st);
 
 // Miss correction (correct.cu): copy each row of the real query's top-k from
@@ -104,8 +116,9 @@ cudaError_t prepare_kernel(Kernel* fn, unsigned long long* done_mask, int dyn_sm
   return cudaSuccess;
 }
 
-// Keys per scoring CTA for a stored dtype and head size (0 if unsupported).
-int score_chunk(int dtype, int head_dim);
+// Keys per scoring CTA for a stored dtype, head size, number of units and
+// keys per unit (0 if the dtype or head size is unsupported).
+int score_chunk(int dtype, int head_dim, long long units, int n);
 
 // Read and clear the device-side status words that kernels set when a bounded
 // wait gives up (nonzero: some wait timed out since the last read).

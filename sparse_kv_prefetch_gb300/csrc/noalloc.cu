@@ -93,7 +93,7 @@ extern "C" dd_status dd_sparse_decode_attn_noalloc(const dd_shape* shape, const 
   if (st != DD_OK) return st;
   char* b = static_cast<char*>(base);
   const cudaError_t e =
-      dd::launch_attn(d, q, k_buf, v_buf, k_dev, v_win, out, reinterpret_cast<float*>(b),
+      dd::launch_attn(d, q, k_buf, v_buf, dd::window_in_cache(k_dev, d), v_win, out, reinterpret_cast<float*>(b),
                       reinterpret_cast<float2*>(b + o_bytes), reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? DD_OK : DD_ERR_CUDA;
 }

@@ -26,7 +26,13 @@ constexpr int kConsumerWarps = 8;
 constexpr int kScoreThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
 constexpr int kStageBytes = 16384;
 constexpr int kStages = 4;
-constexpr int kStagesPerChunk = 16;  // 256 KiB of K per CTA
+// A CTA's chunk is 16 stages (256 KiB of K) when there is enough work; for
+// small layers (few units, short rows, landmark caches) it shrinks by halves,
+// down to the 4 stages of the ring, until the grid has kTargetCtas CTAs, so
+// that the last wave of CTAs is a small share of the launch.
+constexpr int kStagesPerChunk = 16;
+constexpr int kMinStagesPerChunk = 4;
+constexpr long long kTargetCtas = 4096;
 
 // Set when a bounded wait gave up (read and cleared by dd_check_device).
 __device__ unsigned int g_score_status = 0;
@@ -40,7 +46,8 @@ struct ScoreGeom {
   static constexpr int kGroups = kConsumerWarps * kRpw; // row groups per CTA
   static constexpr int kStageRows = kStageBytes / kRowBytes;
   static constexpr int kRowsPerGroup = kStageRows / kGroups;
-  static constexpr int kChunk = kStageRows * kStagesPerChunk;
+  static constexpr int kChunk = kStageRows * kStagesPerChunk;  // rows, at most
+  static constexpr int kMinChunk = kStageRows * kMinStagesPerChunk;
   static_assert(kLpr >= kRowsPerGroup && kLpr <= 32, "unsupported row width");
   static_assert(kStageRows % kGroups == 0, "stage must hold whole row groups");
 };
@@ -51,7 +58,7 @@ template <typename T, int D, int G>
 __global__ void __launch_bounds__(kScoreThreads)
     score_kernel(const uint4* __restrict__ q_spec, const unsigned char* __restrict__ K,
                  float* __restrict__ logits, float2* __restrict__ part, int n, int ldn, int Hq,
-                 int Hkv, int nchunks, float scale) {
+                 int Hkv, int chunk, int nchunks, float scale) {
   using Geo = ScoreGeom<T, D>;
   constexpr int VEC = Geo::kVec, LPR = Geo::kLpr, RPW = Geo::kRpw, NG = Geo::kGroups;
   constexpr int SR = Geo::kStageRows, RPG = Geo::kRowsPerGroup, RB = Geo::kRowBytes;
@@ -69,8 +76,8 @@ __global__ void __launch_bounds__(kScoreThreads)
   const int u = item / nchunks, c = item - u * nchunks;
   const int b = u / Hkv, hk = u - b * Hkv;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int j_begin = c * Geo::kChunk;
-  const int j_end = min(n, j_begin + Geo::kChunk);
+  const int j_begin = c * chunk;
+  const int j_end = min(n, j_begin + chunk);
   const int n_stages = (j_end - j_begin + SR - 1) / SR;
 
   if (threadIdx.x == 0) {
@@ -228,7 +235,7 @@ cudaError_t launch_typed(const Dims& d, const void* q_spec, const void* k_dev, f
   const unsigned grid = (unsigned)d.U * (unsigned)d.nchunks;
   score_kernel<T, D, G><<<grid, kScoreThreads, kScoreSmem, st>>>(
       static_cast<const uint4*>(q_spec), static_cast<const unsigned char*>(k_dev), logits, part,
-      d.n, d.ldn, d.Hq, d.Hkv, d.nchunks, scale);
+      d.n, d.ldn, d.Hq, d.Hkv, d.chunk, d.nchunks, scale);
   return cudaGetLastError();
 }
 
@@ -246,14 +253,24 @@ cudaError_t launch_g(const Dims& d, const void* q, const void* k, float* lg, flo
 
 }  // namespace
 
-int score_chunk(int dtype, int head_dim) {
+namespace {
+template <typename T, int D>
+int chunk_for(long long units, int n) {
+  int rows = ScoreGeom<T, D>::kChunk;
+  while (rows > ScoreGeom<T, D>::kMinChunk && units * ((n + rows - 1) / rows) < kTargetCtas)
+    rows /= 2;
+  return rows;
+}
+}  // namespace
+
+int score_chunk(int dtype, int head_dim, long long units, int n) {
   if (dtype == DD_BF16) {
-    if (head_dim == 64) return ScoreGeom<bf16_t, 64>::kChunk;
-    if (head_dim == 128) return ScoreGeom<bf16_t, 128>::kChunk;
-    if (head_dim == 256) return ScoreGeom<bf16_t, 256>::kChunk;
+    if (head_dim == 64) return chunk_for<bf16_t, 64>(units, n);
+    if (head_dim == 128) return chunk_for<bf16_t, 128>(units, n);
+    if (head_dim == 256) return chunk_for<bf16_t, 256>(units, n);
   } else {
-    if (head_dim == 64) return ScoreGeom<float, 64>::kChunk;
-    if (head_dim == 128) return ScoreGeom<float, 128>::kChunk;
+    if (head_dim == 64) return chunk_for<float, 64>(units, n);
+    if (head_dim == 128) return chunk_for<float, 128>(units, n);
   }
   return 0;
 }

@@ -124,6 +124,14 @@ def test_landmark_sizes():
     assert lib.dd_ctx_set_landmark_chunk(None, 16) == dd.DD_ERR_INVALID_ARG
 
 
+def test_timing_calls_reject_null_context():
+    lib = dd.lib()
+    t = dd.dd_phase_times()
+    assert lib.dd_ctx_set_timing_depth(None, 4) == dd.DD_ERR_INVALID_ARG
+    assert lib.dd_ctx_step_timings(None, 0, ctypes.byref(t)) == dd.DD_ERR_INVALID_ARG
+    assert lib.dd_ctx_timings(None, ctypes.byref(t)) == dd.DD_ERR_INVALID_ARG
+
+
 def test_pageable_host_store_rejected_by_binding():
     import torch
     shp = _shape()

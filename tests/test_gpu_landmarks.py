@@ -158,11 +158,14 @@ def test_chunk_of_identical_keys_has_that_key_as_landmark():
     assert torch.equal(lmk.L.cpu(), want.float())
 
 
-def _layers(w, slots, outs, lms, L):
+def _layers(w, slots, outs, lms, L, k_wins=None):
+    """Layer inputs; with k_wins (one window-key buffer per slot, or None for
+    W = 0) the key cache itself is left out."""
     return [dd.LayerIO(slots[l % len(slots)].q_spec, slots[l % len(slots)].q,
-                       slots[l % len(slots)].K, slots[l % len(slots)].K_h,
-                       slots[l % len(slots)].V_h, slots[l % len(slots)].v_win, outs[l],
-                       lms[l % len(lms)].L)
+                       slots[l % len(slots)].K if k_wins is None else None,
+                       slots[l % len(slots)].K_h, slots[l % len(slots)].V_h,
+                       slots[l % len(slots)].v_win, outs[l], lms[l % len(lms)].L,
+                       None if k_wins is None else k_wins[l % len(slots)])
             for l in range(L)]
 
 
@@ -198,6 +201,17 @@ def test_landmark_decode_step_equals_calls_in_every_schedule(name):
         if sched == "overlap":
             t = ctx.timings()
         runs[sched] = outs
+    # Without the key cache on the device: landmarks plus the window's keys.
+    k_wins = [s.K[:, :, w.ctx_len - w.window:, :].contiguous() if w.window else None
+              for s in slots]
+    for sched, kw in {"overlap_no_k": dict(copy=copy), "serial_no_k": dict(copy=None)}.items():
+        outs = [torch.full((w.batch, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
+                for _ in range(L)]
+        ctx.decode_step(_layers(w, slots, outs, lms, L, k_wins), compute=compute, landmarks=True,
+                        **kw)
+        runs[sched] = outs
+    with pytest.raises(dd.DDError):  # no key cache and no landmark selection
+        ctx.decode_step(_layers(w, slots, outs, lms, L, k_wins), compute=compute)
     torch.cuda.synchronize()
     for sched, outs in runs.items():
         for l in range(L):

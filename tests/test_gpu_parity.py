@@ -194,6 +194,46 @@ def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
     ctx.close()
 
 
+def test_timing_ring_keeps_back_to_back_steps():
+    """With a timing depth of 3, three timed steps enqueued back to back are
+    all readable afterwards; a fourth step pushes the oldest out."""
+    w = SMALL["c2_mini"]
+    slots = [Slot(w)]
+    L = 3
+    outs = [torch.empty((w.batch, w.n_q_heads, w.head_dim), device="cuda") for _ in range(L)]
+    ctx = dd.Ctx(dd_shape(w))
+    layers = dd.Ctx.pack(_layers(w, slots, outs, L))
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    compute.wait_stream(torch.cuda.current_stream())
+    ctx.set_timing_depth(3)
+    for _ in range(3):
+        ctx.decode_step(layers, compute=compute, copy=copy, timing=True)
+    torch.cuda.synchronize()
+    ts = [ctx.timings(back=i) for i in range(3)]
+    for t in ts:
+        assert t["n_layers"] == L and t["launches"] == 6 * L and t["step_ms"] > 0
+        assert 0 < t["score_ms"] <= t["step_ms"]
+    assert all(x > 0 for i in range(3) for x in ctx.score_times(L, back=i))
+    with pytest.raises(dd.DDError):
+        ctx.timings(back=3)
+    ctx.decode_step(layers, compute=compute, copy=None, timing=True)
+    with pytest.raises(dd.DDError):
+        ctx.timings(back=3)
+    assert ctx.timings(back=2)["step_ms"] == ts[1]["step_ms"]  # the former back=1
+    with pytest.raises(dd.DDError):
+        ctx.set_timing_depth(0)
+    # light timing: the step and its scoring phases only, same outputs
+    ref = [o.clone() for o in outs]
+    ctx.decode_step(layers, compute=compute, copy=copy, timing="light")
+    t = ctx.timings()
+    torch.cuda.synchronize()
+    assert t["step_ms"] > 0 and 0 < t["score_ms"] <= t["step_ms"]
+    assert t["gather_ms"] == 0 and t["attn_ms"] == 0 and t["topk_ms"] == 0
+    assert t["launches"] == 6 * L
+    assert all(torch.equal(a, b) for a, b in zip(outs, ref))
+    ctx.close()
+
+
 FULL = {"c2": C2, "c3": C3, "c4": C4, "c5": C5}
 
 
