@@ -35,11 +35,11 @@ import synth  # noqa: E402
 METRIC = "sparse-decode layer-steps/s; scoring HBM GB/s; gather host-link GB/s"
 UNIT = "layer-steps/s"
 FALLBACK_HBM_GBS = 6800.0
-# DRAM read + write bytes of one score_kernel launch, from the ncu capture in
-# profiles/score_kernel_7b32k-batch2.md (batch 2: 546.77 MB for 64 units),
-# scaled by units to the 7B-32K layer (256 units); traffic grows with the
-# units processed.  Keyed by workload; None where no capture exists.
-SCORE_TRAFFIC_BYTES = {"c2-7b-32k": 546.77e6 * 256 / 64}
+# DRAM read + write bytes of one scoring launch, from the ncu captures in
+# profiles/ (batch 2: 64 units), scaled by units to the 7B-32K layer (256
+# units); traffic grows with the units processed.  Keyed by (workload, top-k
+# fused into the scoring kernel); absent where no capture of that kernel exists.
+SCORE_TRAFFIC_BYTES = {("c2-7b-32k", False): 544.71e6 * 256 / 64}
 
 
 def parse():
@@ -68,6 +68,9 @@ def parse():
     p.add_argument("--landmarks", type=int, default=0, metavar="C",
                    help="select whole chunks of C rows by their mean-key landmarks "
                         "(DD_STEP_LANDMARKS) instead of scoring every key; 0: off")
+    p.add_argument("--fused-topk", action="store_true",
+                   help="steps 1-2 as one kernel whose last CTA per unit selects its rows "
+                        "(DD_STEP_FUSED_TOPK) instead of scoring and top-k kernels")
     p.add_argument("--late-gather", type=int, default=0,
                    help="1: start each layer's gather after the previous attention")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -235,7 +238,8 @@ def config_of(w, args):
             "host_store": args.host_alloc, "schedule": args.schedule,
             "copy_stream_priority": args.copy_priority,
             "correct_misses": bool(args.correct_misses),
-            "landmark_chunk": args.landmarks or None}
+            "landmark_chunk": args.landmarks or None,
+            "topk": "fused into scoring" if args.fused_topk else "separate kernel"}
 
 
 def run_reference(args, rank, world):
@@ -440,7 +444,8 @@ def run_ours(args, rank, world):
     def step(copy_stream, timing=True):
         ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
                         late_gather=late, pipeline=pipe, gather_mode=args.gather_mode,
-                        correct_misses=args.correct_misses, landmarks=bool(C))
+                        correct_misses=args.correct_misses, landmarks=bool(C),
+                        fused_topk=args.fused_topk)
 
     def recorded(n_steps):
         """Phase times and per-layer scoring times of the last n timed steps,
@@ -505,7 +510,7 @@ def run_ours(args, rank, world):
             q_l.copy_(q_src, non_blocking=True)
         ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=late, pipeline=pipe,
                         gather_mode=args.gather_mode, correct_misses=args.correct_misses,
-                        landmarks=bool(C))
+                        landmarks=bool(C), fused_topk=args.fused_topk)
         with torch.cuda.stream(compute):
             out_h.copy_(outs, non_blocking=True)
     for _ in range(2):
@@ -575,13 +580,14 @@ def run_ours(args, rank, world):
                                      for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms",
                                                 "attn_ms")},
         "roofline": {"bound": "hbm",
-                     "kernel": ("score_kernel" if not C else
+                     "kernel": ("score_kernel (top-k fused)" if args.fused_topk and not C
+                                else "score_kernel" if not C else
                                 "landmark selection phase (widen q, score, top-k, expand)"),
                      "achieved": score_gbs,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": score_gbs / peak,
                      "traffic": (None if args.profile_case or C
-                                 else SCORE_TRAFFIC_BYTES.get(w.name)),
+                                 else SCORE_TRAFFIC_BYTES.get((w.name, args.fused_topk))),
                      "algorithmic_bytes_per_launch": k_bytes},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT,

@@ -345,6 +345,11 @@ enum {
                               and last events and those around each layer's
                               scoring (selection) phase; dd_ctx_timings then
                               reports step_ms and score_ms only */
+  DD_STEP_FUSED_TOPK = 128, /* one kernel for steps 1-2: the scoring kernel's
+                              last CTA of each unit selects that unit's rows
+                              (no separate top-k launch; same results).  Off by
+                              default: on GB300 the two-kernel form measured
+                              faster on the MHA and GQA workloads */
   DD_STEP_LANDMARKS = 32   /* select with dd_score_topk_landmarks over each
                               layer's `landmarks` instead of scoring every key
                               (chunk set by dd_ctx_set_landmark_chunk; not

@@ -29,6 +29,7 @@ DD_STEP_PIPELINE = 8
 DD_STEP_CORRECT_MISSES = 16
 DD_STEP_LANDMARKS = 32
 DD_STEP_TIMING_LIGHT = 64
+DD_STEP_FUSED_TOPK = 128
 
 
 class DDError(RuntimeError):
@@ -348,7 +349,8 @@ class Ctx:
 
     def decode_step(self, layers, compute=None, copy=None, timing=False,
                     late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False,
-                    correct_misses: bool = False, landmarks: bool = False):
+                    correct_misses: bool = False, landmarks: bool = False,
+                    fused_topk: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
@@ -359,7 +361,8 @@ class Ctx:
                  | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
                  | (DD_STEP_PIPELINE if pipeline else 0)
                  | (DD_STEP_CORRECT_MISSES if correct_misses else 0)
-                 | (DD_STEP_LANDMARKS if landmarks else 0))
+                 | (DD_STEP_LANDMARKS if landmarks else 0)
+                 | (DD_STEP_FUSED_TOPK if fused_topk else 0))
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 

@@ -112,9 +112,29 @@ WsLayout ws_layout(const Dims& d) {
   off += align256((size_t)d.B * d.Hq * d.nsplit * sizeof(float2));
   w.sel_true = off;
   off += align256((size_t)d.U * d.k * sizeof(float));
+  w.counters = off;
+  off += align256((size_t)d.U * sizeof(int32_t));
   w.total = off;
   return w;
 }
+
+cudaError_t select_rows(const Dims& d, const WsLayout& lay, char* ws, const void* q,
+                        const void* k_dev, int32_t* idx, float* sel, float* lse, bool fused,
+                        cudaStream_t st, int* launches) {
+  float* logits = reinterpret_cast<float*>(ws + lay.logits);
+  float2* part = reinterpret_cast<float2*>(ws + lay.part);
+  if (fused) {
+    *launches += kScoreSelectLaunches;
+    return launch_score_select(d, q, k_dev, logits, part,
+                               reinterpret_cast<int32_t*>(ws + lay.counters), idx, sel, lse, st);
+  }
+  *launches += kScoreLaunches + kTopkLaunches;
+  cudaError_t e = launch_score(d, q, k_dev, logits, part, st);
+  if (e == cudaSuccess) e = launch_topk(d, logits, part, idx, sel, lse, st);
+  return e;
+}
+
+
 
 dd_status resolve_landmarks(const dd_shape* s, int chunk, LandmarkDims* out) {
   Dims f;
@@ -297,11 +317,9 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
     return DD_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* logits = reinterpret_cast<float*>(ws + w.logits);
-  float2* part = reinterpret_cast<float2*>(ws + w.part);
-  st = cuda_status(launch_score(d, q_spec, k_dev, logits, part, s));
-  if (st != DD_OK) return st;
-  return cuda_status(launch_topk(d, logits, part, idx_out, sel_score_out, lse_out, s));
+  int launches = 0;
+  return cuda_status(
+      select_rows(d, w, ws, q_spec, k_dev, idx_out, sel_score_out, lse_out, false, s, &launches));
 }
 
 dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v_host,
@@ -371,12 +389,10 @@ dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_
     return DD_ERR_INVALID_ARG;
   char* ws = static_cast<char*>(workspace);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  float* logits = reinterpret_cast<float*>(ws + w.logits);
-  float2* part = reinterpret_cast<float2*>(ws + w.part);
   float* sel_true = reinterpret_cast<float*>(ws + w.sel_true);
-  st = cuda_status(launch_score(d, q, k_dev, logits, part, s));
-  if (st != DD_OK) return st;
-  st = cuda_status(launch_topk(d, logits, part, idx_true_out, sel_true, nullptr, s));
+  int launches = 0;
+  st = cuda_status(
+      select_rows(d, w, ws, q, k_dev, idx_true_out, sel_true, nullptr, false, s, &launches));
   if (st != DD_OK) return st;
   return cuda_status(launch_fixup(d, idx_spec, idx_true_out, sel_true, k_buf_spec, v_buf_spec, kh,
                                   vh, k_buf_out, v_buf_out, miss_out, mass_out, s));
@@ -414,8 +430,10 @@ dd_status dd_build_landmarks(const dd_shape* shape, int chunk, const void* k_dev
 
 namespace {
 // Landmark selection into `rows` (the k expanded rows) and `sel` (chunk scores).
+// The fused selection's counters in `ws` must be zero (they are after it).
 cudaError_t landmark_select(const LandmarkDims& L, const void* q, const void* landmarks,
-                            int32_t* rows, float* sel, float* lse, char* ws, cudaStream_t st) {
+                            int32_t* rows, float* sel, float* lse, char* ws, bool fused,
+                            cudaStream_t st, int* launches) {
   const Dims& f = L.full;
   const float* q32 = static_cast<const float*>(q);
   if (f.dtype == DD_BF16) {
@@ -423,13 +441,13 @@ cudaError_t landmark_select(const LandmarkDims& L, const void* q, const void* la
     cudaError_t e = launch_to_f32(q, tmp, f.B * f.Hq * f.d, st);
     if (e != cudaSuccess) return e;
     q32 = tmp;
+    ++*launches;
   }
-  float* logits = reinterpret_cast<float*>(ws + L.lay.logits);
-  float2* part = reinterpret_cast<float2*>(ws + L.lay.part);
   int32_t* chunks = reinterpret_cast<int32_t*>(ws + L.chunks);
-  cudaError_t e = launch_score(L.lm, q32, landmarks, logits, part, st);
-  if (e == cudaSuccess) e = launch_topk(L.lm, logits, part, chunks, sel, lse, st);
+  cudaError_t e = select_rows(L.lm, L.lay, ws, q32, landmarks, chunks, sel, lse, fused, st,
+                              launches);
   if (e == cudaSuccess) e = launch_expand(chunks, rows, f.U, L.lm.k, L.chunk, st);
+  ++*launches;
   return e;
 }
 }  // namespace
@@ -448,9 +466,11 @@ dd_status dd_score_topk_landmarks(const dd_shape* shape, int chunk, const void* 
   if (ws_bytes < L.total) return DD_ERR_INVALID_ARG;
   if (!all_device({q_spec, landmarks, idx_out, chunk_score_out, lse_out, workspace}))
     return DD_ERR_INVALID_ARG;
-  return cuda_status(landmark_select(L, q_spec, landmarks, idx_out, chunk_score_out, lse_out,
-                                     static_cast<char*>(workspace),
-                                     reinterpret_cast<cudaStream_t>(stream)));
+  char* ws = static_cast<char*>(workspace);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  int launches = 0;
+  return cuda_status(landmark_select(L, q_spec, landmarks, idx_out, chunk_score_out, lse_out, ws,
+                                     false, s, &launches));
 }
 
 }  // extern "C"
@@ -630,6 +650,10 @@ dd_status dd_ctx_create(const dd_shape* shape, dd_ctx** out) {
   }
   ok = ok && cudaMalloc((void**)&c->lse, (size_t)d.B * d.Hq * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&c->ws, c->ws_lay.total) == cudaSuccess;
+  // The fused selection's counters start at zero (each launch leaves them so).
+  ok = ok && cudaMemset(static_cast<char*>(c->ws) + c->ws_lay.counters, 0,
+                        (size_t)d.U * sizeof(int32_t)) == cudaSuccess &&
+       cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     ctx_free(c);
@@ -674,6 +698,10 @@ dd_status dd_ctx_set_landmark_chunk(dd_ctx* c, int chunk) {
       cudaGetLastError();
       return DD_ERR_OOM;
     }
+    if (cudaMemset(static_cast<char*>(c->lm_ws) + L.lay.counters, 0,
+                   (size_t)L.lm.U * sizeof(int32_t)) != cudaSuccess ||
+        cudaDeviceSynchronize() != cudaSuccess)
+      return DD_ERR_CUDA;
     c->device_bytes += L.total;
   } else {
     L.total = have;  // keep the larger buffer's size on record
@@ -713,6 +741,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   const int gather_mode = (flags & DD_STEP_GATHER_LSU) ? 1 : 0;
   const bool correct = (flags & DD_STEP_CORRECT_MISSES) != 0;
   const bool use_lm = (flags & DD_STEP_LANDMARKS) != 0;
+  const bool fused = (flags & DD_STEP_FUSED_TOPK) != 0;
   if (use_lm) {
     if (c->lm_chunk == 0 || correct) return DD_ERR_UNSUPPORTED;
     for (int l = 0; l < n_layers; ++l) {
@@ -757,11 +786,20 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     if (use_lm) {
       // Landmark selection: phase "score" covers it all, "top-k" is empty.
       cudaError_t e = landmark_select(c->lm, layers[l].q_spec, layers[l].landmarks, c->idx[s],
-                                      c->sel[s], c->lse, static_cast<char*>(c->lm_ws), C);
+                                      c->sel[s], c->lse, static_cast<char*>(c->lm_ws), fused, C,
+                                      &launches);
       if (e != cudaSuccess) return e;
       if (timing) cudaEventRecord(T(l, PH_SCORE1), C);
       if (phases) cudaEventRecord(T(l, PH_TOPK1), C);
-      launches += (d.dtype == DD_BF16 ? 1 : 0) + kScoreLaunches + kTopkLaunches + 1;
+      return cudaEventRecord(c->ev_idx[s], C);
+    }
+    if (fused) {
+      // DD_STEP_FUSED_TOPK: one kernel, phase "score" covers the selection.
+      cudaError_t e = select_rows(d, c->ws_lay, ws, layers[l].q_spec, layers[l].k_dev, c->idx[s],
+                                  c->sel[s], c->lse, true, C, &launches);
+      if (e != cudaSuccess) return e;
+      if (timing) cudaEventRecord(T(l, PH_SCORE1), C);
+      if (phases) cudaEventRecord(T(l, PH_TOPK1), C);
       return cudaEventRecord(c->ev_idx[s], C);
     }
     cudaError_t e = launch_score(d, layers[l].q_spec, layers[l].k_dev, logits, part, C);
@@ -808,14 +846,14 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     if (correct) {
       // The real query's own top-k; rows the prediction missed come from host.
       float* sel_true = reinterpret_cast<float*>(ws + c->ws_lay.sel_true);
-      e = launch_score(d, layers[l].q, layers[l].k_dev, logits, part, A);
-      if (e == cudaSuccess) e = launch_topk(d, logits, part, c->idx_true, sel_true, nullptr, A);
+      e = select_rows(d, c->ws_lay, ws, layers[l].q, layers[l].k_dev, c->idx_true, sel_true,
+                      nullptr, fused, A, &launches);
       if (e == cudaSuccess)
         e = launch_fixup(d, c->idx[s], c->idx_true, sel_true, c->kbuf[s], c->vbuf[s], kh[l], vh[l],
                          c->kb_true, c->vb_true, c->miss + (size_t)l * d.U,
                          c->mass + (size_t)l * d.U * 2, A);
       if (e != cudaSuccess) return e;
-      launches += kScoreLaunches + kTopkLaunches + kFixupLaunches;
+      launches += kFixupLaunches;
       kb = c->kb_true;
       vb = c->vb_true;
     }

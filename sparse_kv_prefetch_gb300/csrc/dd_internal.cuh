@@ -23,7 +23,7 @@ struct Dims {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t logits, part, attn_o, attn_ml, sel_true, total;
+  size_t logits, part, attn_o, attn_ml, sel_true, counters, total;
 };
 
 dd_status resolve(const dd_shape* s, Dims* out);
@@ -37,6 +37,11 @@ cudaError_t launch_score(const Dims& d, const void* q_spec, const void* k_dev, f
                          float2* part, cudaStream_t st);
 cudaError_t launch_topk(const Dims& d, const float* logits, const float2* part, int32_t* idx,
                         float* sel, float* lse, cudaStream_t st);
+// Scoring with the selection fused in: the last CTA of each unit runs its
+// top-k.  counters [U] must be zero before the launch and are zero after it.
+cudaError_t launch_score_select(const Dims& d, const void* q_spec, const void* k_dev,
+                                float* logits, float2* part, int32_t* counters, int32_t* idx,
+                                float* sel, float* lse, cudaStream_t st);
 cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
                           const int32_t* idx, void* k_buf, void* v_buf, int mode,
                           cudaStream_t st);
@@ -85,7 +90,15 @@ dd_status resolve_landmarks(const dd_shape* s, int chunk, LandmarkDims* out);
 
 // Number of kernels each launcher enqueues.
 constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 2, kAttnLaunches = 2,
-              kFixupLaunches = 1;
+              kFixupLaunches = 1, kScoreSelectLaunches = 1;
+
+// Steps 1-2 of one layer into idx / sel / lse, with the workspace laid out by
+// `lay`: the fused kernel (counters at lay.counters must be zero) or, if
+// !fused, the scoring and top-k kernels.  Adds the kernels launched to
+// *launches.
+cudaError_t select_rows(const Dims& d, const WsLayout& lay, char* ws, const void* q,
+                        const void* k_dev, int32_t* idx, float* sel, float* lse, bool fused,
+                        cudaStream_t st, int* launches);
 
 // Huge-page size of the host (transparent huge pages), read once; 2 MiB if
 // the host does not report one.  Host stores from dd_host_alloc use it.
@@ -229,6 +242,21 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, 
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
           smem_addr(smem_dst)),
       "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+// An L2 policy that evicts the lines it tags first (for data read once).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// bulk_load with an L2 cache policy for the source lines.
+__device__ __forceinline__ void bulk_load_hint(void* smem_dst, const void* gmem_src,
+                                               uint32_t bytes, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
 // shared -> global, tracked by the issuing thread's bulk async-groups.

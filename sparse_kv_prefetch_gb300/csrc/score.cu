@@ -18,6 +18,7 @@
 #include <math.h>
 
 #include "dd_internal.cuh"
+#include "select.cuh"
 
 namespace dd {
 namespace {
@@ -52,13 +53,31 @@ struct ScoreGeom {
   static_assert(kStageRows % kGroups == 0, "stage must hold whole row groups");
 };
 
-constexpr size_t kScoreSmem = (size_t)kStages * kStageBytes + 2 * kStages * sizeof(uint64_t);
+// Fused selection: the last CTA of a unit to finish runs the unit's top-k
+// with its eight consumer warps, reusing the ring's shared memory.
+constexpr int kSelWarps = kConsumerWarps;
+constexpr int kSelCap = 1024;  // list entries per warp
+using SelSmem = sel::Smem<kSelWarps, kSelCap>;
+constexpr size_t kRingBytes = (size_t)kStages * kStageBytes;
+constexpr size_t kRegionBytes =
+    ((kRingBytes > sizeof(SelSmem) ? kRingBytes : sizeof(SelSmem)) + 127) / 128 * 128;
+// [0, kRegionBytes): the ring, later the selection's lists; then the mbarriers.
+constexpr size_t kScoreSmem = kRegionBytes + 2 * kStages * sizeof(uint64_t);
 
-template <typename T, int D, int G>
+// Selection outputs of the fused kernel (unused when FUSED is false).
+struct FusedOut {
+  int32_t* counters;  // [U], zero before the launch; each unit's last CTA re-zeroes its own
+  int32_t* idx;       // [U][k]
+  float* sel;         // [U][k]
+  float* lse;         // [B][H_q] or NULL
+  int span, k;
+};
+
+template <typename T, int D, int G, bool FUSED>
 __global__ void __launch_bounds__(kScoreThreads)
     score_kernel(const uint4* __restrict__ q_spec, const unsigned char* __restrict__ K,
                  float* __restrict__ logits, float2* __restrict__ part, int n, int ldn, int Hq,
-                 int Hkv, int chunk, int nchunks, float scale) {
+                 int Hkv, int chunk, int nchunks, float scale, FusedOut fo) {
   using Geo = ScoreGeom<T, D>;
   constexpr int VEC = Geo::kVec, LPR = Geo::kLpr, RPW = Geo::kRpw, NG = Geo::kGroups;
   constexpr int SR = Geo::kStageRows, RPG = Geo::kRowsPerGroup, RB = Geo::kRowBytes;
@@ -69,7 +88,7 @@ __global__ void __launch_bounds__(kScoreThreads)
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)kStages * kStageBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRegionBytes);
   uint64_t* empty = full + kStages;
 
   const int item = blockIdx.x;
@@ -98,6 +117,9 @@ __global__ void __launch_bounds__(kScoreThreads)
   if (warp == kConsumerWarps) {
     // Producer: one lane keeps up to kStages bulk copies in flight.
     if (lane == 0) {
+      // K is read once: its lines go first when L2 needs room, so the logits
+      // written by this launch stay there for the selection that reads them.
+      const uint64_t policy = l2_evict_first_policy();
       for (int t = 0; t < n_stages; ++t) {
         const int s = t % kStages;
         if (t >= kStages && !mbar_wait(&empty[s], ((t / kStages) - 1) & 1)) {
@@ -107,8 +129,8 @@ __global__ void __launch_bounds__(kScoreThreads)
         const int r0 = j_begin + t * SR;
         const int nr = min(SR, j_end - r0);
         mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * RB));
-        bulk_load(ring + (size_t)s * kStageBytes, Ku + (size_t)r0 * RB, (uint32_t)(nr * RB),
-                  &full[s]);
+        bulk_load_hint(ring + (size_t)s * kStageBytes, Ku + (size_t)r0 * RB,
+                       (uint32_t)(nr * RB), &full[s], policy);
       }
     }
   } else {
@@ -223,30 +245,64 @@ __global__ void __launch_bounds__(kScoreThreads)
     for (int w = 1; w <= kConsumerWarps; ++w) p = lse_merge(p, red[g][w]);
     part[(size_t)(u * G + g) * nchunks + c] = p;
   }
+  if (!FUSED) return;
+
+  // Fused selection.  Every thread fences its logits and (max, sum) pair,
+  // then one thread counts the CTA in; the CTA that completes the unit's
+  // count (all others have fenced and counted before) selects its top-k.
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(fo.counters + u, 1) == nchunks - 1;
+  __syncthreads();
+  if (!s_last || warp == kConsumerWarps) return;  // the producer warp is not needed
+  __threadfence();
+  if (threadIdx.x == 0) fo.counters[u] = 0;  // ready for the next launch
+  // Every bulk copy into the ring has landed (all stages were waited for), so
+  // its memory can hold the selection's histogram and lists.
+  SelSmem& sm = *reinterpret_cast<SelSmem*>(smem);
+  sel::merge_lse<G, true>(part, u, b, hk, Hq, nchunks, fo.lse, sm);
+  sel::sync<kSelWarps>();
+  sel::select_unit<G, true>(sm, logits + (size_t)(b * Hq + hk * G) * ldn, ldn, fo.span, fo.k,
+                            fo.idx + (size_t)u * fo.k, fo.sel + (size_t)u * fo.k);
 }
 
-template <typename T, int D, int G>
+template <typename T, int D, int G, bool FUSED>
 cudaError_t launch_typed(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
-                         float2* part, cudaStream_t st) {
+                         float2* part, const FusedOut& fo, cudaStream_t st) {
   static unsigned long long prepared = 0;
-  cudaError_t e = prepare_kernel(score_kernel<T, D, G>, &prepared, (int)kScoreSmem);
+  cudaError_t e = prepare_kernel(score_kernel<T, D, G, FUSED>, &prepared, (int)kScoreSmem);
   if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)d.d);
   const unsigned grid = (unsigned)d.U * (unsigned)d.nchunks;
-  score_kernel<T, D, G><<<grid, kScoreThreads, kScoreSmem, st>>>(
+  score_kernel<T, D, G, FUSED><<<grid, kScoreThreads, kScoreSmem, st>>>(
       static_cast<const uint4*>(q_spec), static_cast<const unsigned char*>(k_dev), logits, part,
-      d.n, d.ldn, d.Hq, d.Hkv, d.chunk, d.nchunks, scale);
+      d.n, d.ldn, d.Hq, d.Hkv, d.chunk, d.nchunks, scale, fo);
   return cudaGetLastError();
 }
 
-template <typename T, int D>
+template <typename T, int D, bool FUSED>
 cudaError_t launch_g(const Dims& d, const void* q, const void* k, float* lg, float2* p,
-                     cudaStream_t st) {
+                     const FusedOut& fo, cudaStream_t st) {
   switch (d.G) {
-    case 1: return launch_typed<T, D, 1>(d, q, k, lg, p, st);
-    case 2: return launch_typed<T, D, 2>(d, q, k, lg, p, st);
-    case 4: return launch_typed<T, D, 4>(d, q, k, lg, p, st);
-    case 8: return launch_typed<T, D, 8>(d, q, k, lg, p, st);
+    case 1: return launch_typed<T, D, 1, FUSED>(d, q, k, lg, p, fo, st);
+    case 2: return launch_typed<T, D, 2, FUSED>(d, q, k, lg, p, fo, st);
+    case 4: return launch_typed<T, D, 4, FUSED>(d, q, k, lg, p, fo, st);
+    case 8: return launch_typed<T, D, 8, FUSED>(d, q, k, lg, p, fo, st);
+  }
+  return cudaErrorInvalidValue;
+}
+
+template <bool FUSED>
+cudaError_t launch_any(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
+                       float2* part, const FusedOut& fo, cudaStream_t st) {
+  if (d.dtype == DD_BF16) {
+    if (d.d == 64) return launch_g<bf16_t, 64, FUSED>(d, q_spec, k_dev, logits, part, fo, st);
+    if (d.d == 128) return launch_g<bf16_t, 128, FUSED>(d, q_spec, k_dev, logits, part, fo, st);
+    if (d.d == 256) return launch_g<bf16_t, 256, FUSED>(d, q_spec, k_dev, logits, part, fo, st);
+  } else {
+    if (d.d == 64) return launch_g<float, 64, FUSED>(d, q_spec, k_dev, logits, part, fo, st);
+    if (d.d == 128) return launch_g<float, 128, FUSED>(d, q_spec, k_dev, logits, part, fo, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -277,15 +333,14 @@ int score_chunk(int dtype, int head_dim, long long units, int n) {
 
 cudaError_t launch_score(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
                          float2* part, cudaStream_t st) {
-  if (d.dtype == DD_BF16) {
-    if (d.d == 64) return launch_g<bf16_t, 64>(d, q_spec, k_dev, logits, part, st);
-    if (d.d == 128) return launch_g<bf16_t, 128>(d, q_spec, k_dev, logits, part, st);
-    if (d.d == 256) return launch_g<bf16_t, 256>(d, q_spec, k_dev, logits, part, st);
-  } else {
-    if (d.d == 64) return launch_g<float, 64>(d, q_spec, k_dev, logits, part, st);
-    if (d.d == 128) return launch_g<float, 128>(d, q_spec, k_dev, logits, part, st);
-  }
-  return cudaErrorInvalidValue;
+  return launch_any<false>(d, q_spec, k_dev, logits, part, FusedOut{}, st);
+}
+
+cudaError_t launch_score_select(const Dims& d, const void* q_spec, const void* k_dev,
+                                float* logits, float2* part, int32_t* counters, int32_t* idx,
+                                float* sel, float* lse, cudaStream_t st) {
+  const FusedOut fo{counters, idx, sel, lse, d.span, d.k};
+  return launch_any<true>(d, q_spec, k_dev, logits, part, fo, st);
 }
 
 unsigned int take_score_status() {

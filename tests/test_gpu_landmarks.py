@@ -194,7 +194,8 @@ def test_landmark_decode_step_equals_calls_in_every_schedule(name):
     for sched, kw in {"overlap": dict(copy=copy, timing=True), "serial": dict(copy=None),
                       "late": dict(copy=copy, late_gather=True),
                       "pipeline": dict(copy=copy, pipeline=True),
-                      "lsu": dict(copy=copy, gather_mode=1)}.items():
+                      "lsu": dict(copy=copy, gather_mode=1),
+                      "fused": dict(copy=copy, fused_topk=True)}.items():
         outs = [torch.full((w.batch, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
                 for _ in range(L)]
         ctx.decode_step(_layers(w, slots, outs, lms, L), compute=compute, landmarks=True, **kw)
@@ -216,6 +217,7 @@ def test_landmark_decode_step_equals_calls_in_every_schedule(name):
     for sched, outs in runs.items():
         for l in range(L):
             assert torch.equal(outs[l], ref[l % D]), f"{sched}, layer {l}: != standalone calls"
+    # widen q (bf16), score, top-k, expand, gather (2), attention (2)
     per_layer = (1 if w.dtype == synth.BF16 else 0) + 1 + 1 + 1 + 2 + 2
     assert t["n_layers"] == L and t["launches"] == L * per_layer
     with pytest.raises(dd.DDError):  # not combinable with miss correction

@@ -182,14 +182,47 @@ def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
     ctx.decode_step(_layers(w, slots, outs_c, L), compute=compute, copy=copy, late_gather=True)
     outs_d = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
     ctx.decode_step(_layers(w, slots, outs_d, L), compute=compute, copy=copy, pipeline=True)
+    # steps 1-2 as one kernel (the scoring kernel's last CTA per unit selects)
+    outs_e = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
+    ctx.decode_step(_layers(w, slots, outs_e, L), compute=compute, copy=copy, fused_topk=True,
+                    timing=True)
+    t_fused = ctx.timings()
+    outs_f = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
+    ctx.decode_step(_layers(w, slots, outs_f, L), compute=compute, copy=None, fused_topk=True)
     torch.cuda.synchronize()
     for l in range(L):
         assert torch.equal(outs_a[l], outs_b[l]), f"layer {l}: overlapped != serial"
         assert torch.equal(outs_c[l], outs_b[l]), f"layer {l}: late gather != serial"
         assert torch.equal(outs_d[l], outs_b[l]), f"layer {l}: pipeline != serial"
+        assert torch.equal(outs_e[l], outs_b[l]), f"layer {l}: fused top-k != two kernels"
+        assert torch.equal(outs_f[l], outs_b[l]), f"layer {l}: fused serial != two kernels"
         assert torch.equal(outs_a[l], ref[l % D]), f"layer {l}: step != per-layer calls"
-    assert t["n_layers"] == L and t["launches"] == L * 6
+    assert t["n_layers"] == L and t["launches"] == L * 6 and t["topk_ms"] > 0
+    assert t_fused["launches"] == L * 5
     assert t["step_ms"] > 0 and t["score_ms"] > 0 and t["gather_ms"] > 0
+    dd.check_device()
+    ctx.close()
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_fused_selection_equals_two_kernels(name):
+    """Steps 1-2 as one kernel (the scoring kernel's last CTA of each unit
+    selects its rows) give the same indices and outputs, bit for bit, as the
+    scoring and top-k kernels, for every head size, group size and dtype."""
+    w = SMALL[name]
+    slots = [Slot(w)]
+    L = 2
+    ctx = dd.Ctx(dd_shape(w))
+    runs = []
+    for fused in (False, True, False, True):  # repeated: the counters reset themselves
+        outs = [torch.full((w.batch, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
+                for _ in range(L)]
+        ctx.decode_step(_layers(w, slots, outs, L), fused_topk=fused)
+        runs.append(outs)
+    torch.cuda.synchronize()
+    for r in runs[1:]:
+        for l in range(L):
+            assert torch.equal(r[l], runs[0][l])
     dd.check_device()
     ctx.close()
 
