@@ -479,6 +479,17 @@ def run_ours(args, rank, world):
     timed, score_ms = recorded(args.steps)
     launches = sum(t["launches"] for t in timed)
 
+    # The same steps without any per-layer events (only the two around the
+    # region): what the instrumentation of the timed region costs.
+    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev2.record(compute)
+    for _ in range(args.steps):
+        step(copy, timing=False)
+    ev3.record(compute)
+    torch.cuda.synchronize()
+    bare_s = max_over_ranks(ev2.elapsed_time(ev3) * 1e-3, world)
+    value_bare = job_throughput(L, args.steps, bare_s, world)
+
     # Phase breakdown: the same steps with events around every phase.
     for _ in range(n_phase):
         step(copy)
@@ -576,6 +587,9 @@ def run_ours(args, rank, world):
                               for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms", "attn_ms")},
         "serial_step_ms": t_ser,
         "timed_step_ms_median": statistics.median(p["step_ms"] for p in timed),
+        "value_without_layer_events": value_bare,
+        "value_without_layer_events_what": "the same K steps right after the timed region, "
+                                           "with no events inside the steps",
         "serial_phase_ms_per_step": {kk: statistics.mean(p[kk] for p in serial)
                                      for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms",
                                                 "attn_ms")},

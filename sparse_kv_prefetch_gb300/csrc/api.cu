@@ -435,6 +435,18 @@ cudaError_t landmark_select(const LandmarkDims& L, const void* q, const void* la
                             int32_t* rows, float* sel, float* lse, char* ws, bool fused,
                             cudaStream_t st, int* launches) {
   const Dims& f = L.full;
+  if (!fused) {
+    // Scoring reads the bf16 query itself; the top-k writes each selected
+    // chunk's rows.
+    float* logits = reinterpret_cast<float*>(ws + L.lay.logits);
+    float2* part = reinterpret_cast<float2*>(ws + L.lay.part);
+    cudaError_t e = f.dtype == DD_BF16
+                        ? launch_score_bf16_query(L.lm, q, landmarks, logits, part, st)
+                        : launch_score(L.lm, q, landmarks, logits, part, st);
+    if (e == cudaSuccess) e = launch_topk(L.lm, logits, part, rows, sel, lse, st, L.chunk);
+    *launches += kScoreLaunches + kTopkLaunches;
+    return e;
+  }
   const float* q32 = static_cast<const float*>(q);
   if (f.dtype == DD_BF16) {
     float* tmp = reinterpret_cast<float*>(ws + L.q32);

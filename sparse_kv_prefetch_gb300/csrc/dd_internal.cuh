@@ -35,8 +35,13 @@ constexpr int kAttnRowsPerSplit = 64;
 // launch status (cudaGetLastError after the launch).
 cudaError_t launch_score(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
                          float2* part, cudaStream_t st);
+// With expand = c > 1 each selected position j is written as the c rows
+// j c .. j c + c - 1 (idx is then [U][k c]); sel stays [U][k].
 cudaError_t launch_topk(const Dims& d, const float* logits, const float2* part, int32_t* idx,
-                        float* sel, float* lse, cudaStream_t st);
+                        float* sel, float* lse, cudaStream_t st, int expand = 1);
+// Scoring of fp32 keys (landmarks, d.dtype == DD_F32) by a bf16 query.
+cudaError_t launch_score_bf16_query(const Dims& d, const void* q_bf16, const void* k_f32,
+                                    float* logits, float2* part, cudaStream_t st);
 // Scoring with the selection fused in: the last CTA of each unit runs its
 // top-k.  counters [U] must be zero before the launch and are zero after it.
 cudaError_t launch_score_select(const Dims& d, const void* q_spec, const void* k_dev,

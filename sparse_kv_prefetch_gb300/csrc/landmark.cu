@@ -5,14 +5,17 @@
 // their entries from host memory.  Here a landmark is the mean key of a chunk
 // of c adjacent positions of [0, n - W), kept in fp32 in HBM (c times smaller
 // than K in elements).  Selection scores the landmarks with the scoring and
-// top-k kernels (as a key cache of M = (n - W) / c rows), then expands the
-// k / c selected chunks to their k rows, which the gather then moves as runs
-// of c contiguous rows.
+// top-k kernels (as a key cache of M = (n - W) / c rows; the scoring kernel
+// widens a bf16 query itself) and the top-k writes each of the k / c selected
+// chunks as its c rows, which the gather then moves as runs of c contiguous
+// rows.
 //
 // landmark_kernel: one thread per (unit, chunk, 16-byte piece of a row); it
 //   sums the piece over the chunk's c rows in fp32 and divides by c.
+// For the fused form of steps 1-2 (DD_STEP_FUSED_TOPK), whose scoring kernel
+// takes an fp32 query and writes chunk ids:
+// to_f32_kernel: widens bf16 queries to fp32;
 // expand_kernel: rows[u][i c + r] = chunk[u][i] c + r.
-// to_f32_kernel: widens bf16 queries to fp32 for the fp32 landmark scoring.
 #include "dd_internal.cuh"
 
 namespace dd {

@@ -73,7 +73,9 @@ struct FusedOut {
   int span, k;
 };
 
-template <typename T, int D, int G, bool FUSED>
+// QB: the keys are fp32 (landmarks) but the query is bf16; it is widened
+// exactly on load.
+template <typename T, int D, int G, bool FUSED, bool QB = false>
 __global__ void __launch_bounds__(kScoreThreads)
     score_kernel(const uint4* __restrict__ q_spec, const unsigned char* __restrict__ K,
                  float* __restrict__ logits, float2* __restrict__ part, int n, int ldn, int Hq,
@@ -138,8 +140,19 @@ __global__ void __launch_bounds__(kScoreThreads)
     const int grp = warp * RPW + lane / LPR;
     float qf[G][VEC];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      unpack(ld_ro(q_spec + ((size_t)(b * Hq + hk * G + g)) * LPR + sub), qf[g]);
+    for (int g = 0; g < G; ++g) {
+      const size_t piece = (size_t)(b * Hq + hk * G + g) * LPR + sub;
+      if constexpr (QB) {
+        static_assert(VEC == 4, "a bf16 query widens to fp32 keys only");
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(q_spec) + piece);
+        qf[g][0] = __uint_as_float(v.x << 16);
+        qf[g][1] = __uint_as_float(v.x & 0xFFFF0000u);
+        qf[g][2] = __uint_as_float(v.y << 16);
+        qf[g][3] = __uint_as_float(v.y & 0xFFFF0000u);
+      } else {
+        unpack(ld_ro(q_spec + piece), qf[g]);
+      }
+    }
 
     // After the transposed reduction below, lane `sub` holds the totals of
     // the P values with indices prefix*P + p (p < P), index = g*RPG + i for
@@ -267,15 +280,15 @@ __global__ void __launch_bounds__(kScoreThreads)
                             fo.idx + (size_t)u * fo.k, fo.sel + (size_t)u * fo.k);
 }
 
-template <typename T, int D, int G, bool FUSED>
+template <typename T, int D, int G, bool FUSED, bool QB = false>
 cudaError_t launch_typed(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
                          float2* part, const FusedOut& fo, cudaStream_t st) {
   static unsigned long long prepared = 0;
-  cudaError_t e = prepare_kernel(score_kernel<T, D, G, FUSED>, &prepared, (int)kScoreSmem);
+  cudaError_t e = prepare_kernel(score_kernel<T, D, G, FUSED, QB>, &prepared, (int)kScoreSmem);
   if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)d.d);
   const unsigned grid = (unsigned)d.U * (unsigned)d.nchunks;
-  score_kernel<T, D, G, FUSED><<<grid, kScoreThreads, kScoreSmem, st>>>(
+  score_kernel<T, D, G, FUSED, QB><<<grid, kScoreThreads, kScoreSmem, st>>>(
       static_cast<const uint4*>(q_spec), static_cast<const unsigned char*>(k_dev), logits, part,
       d.n, d.ldn, d.Hq, d.Hkv, d.chunk, d.nchunks, scale, fo);
   return cudaGetLastError();
@@ -334,6 +347,23 @@ int score_chunk(int dtype, int head_dim, long long units, int n) {
 cudaError_t launch_score(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
                          float2* part, cudaStream_t st) {
   return launch_any<false>(d, q_spec, k_dev, logits, part, FusedOut{}, st);
+}
+
+cudaError_t launch_score_bf16_query(const Dims& d, const void* q_bf16, const void* k_f32,
+                                    float* logits, float2* part, cudaStream_t st) {
+  if (d.dtype != DD_F32) return cudaErrorInvalidValue;
+  const FusedOut fo{};
+  switch (d.d * 16 + d.G) {
+    case 64 * 16 + 1: return launch_typed<float, 64, 1, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+    case 64 * 16 + 2: return launch_typed<float, 64, 2, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+    case 64 * 16 + 4: return launch_typed<float, 64, 4, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+    case 64 * 16 + 8: return launch_typed<float, 64, 8, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+    case 128 * 16 + 1: return launch_typed<float, 128, 1, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+    case 128 * 16 + 2: return launch_typed<float, 128, 2, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+    case 128 * 16 + 4: return launch_typed<float, 128, 4, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+    case 128 * 16 + 8: return launch_typed<float, 128, 8, false, true>(d, q_bf16, k_f32, logits, part, fo, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_score_select(const Dims& d, const void* q_spec, const void* k_dev,

@@ -206,6 +206,17 @@ __device__ void histogram_lists(Smem<WARPS, WCAP>& sm, int lo, int nbits, uint32
   sync<WARPS>();
 }
 
+// Index written for a selected position j: j itself, or with expand = c > 1
+// (landmark selection, where j is a chunk) the c rows j c .. j c + c - 1 of
+// the chunk, at slots pos c .. pos c + c - 1.
+__device__ __forceinline__ void put_index(int32_t* idx_out, int pos, int j, int expand) {
+  if (expand == 1) {
+    idx_out[pos] = j;
+  } else {
+    for (int r = 0; r < expand; ++r) idx_out[pos * expand + r] = j * expand + r;
+  }
+}
+
 // Score written for a selected key: alpha (MHA) or the group score itself.
 __device__ __forceinline__ float sel_value(uint32_t key, bool mha, float lse0) {
   const float v = key2f(key);
@@ -216,7 +227,7 @@ __device__ __forceinline__ float sel_value(uint32_t key, bool mha, float lse0) {
 // keys == T in position order.
 template <int WARPS, int WCAP>
 __device__ void emit_lists(Smem<WARPS, WCAP>& sm, uint32_t T, uint32_t k_rem, int k,
-                           int32_t* idx_out, float* sel_out, bool mha, float lse0) {
+                           int32_t* idx_out, float* sel_out, bool mha, float lse0, int expand) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const uint32_t* keys = sm.keys + warp * WCAP;
   const int32_t* idxs = sm.idxs + warp * WCAP;
@@ -259,7 +270,7 @@ __device__ void emit_lists(Smem<WARPS, WCAP>& sm, uint32_t T, uint32_t k_rem, in
     if (gt) pos = (int)(g_before + min(q_before, k_rem));
     else if (eq && q_before < k_rem) pos = (int)(g_before + q_before);
     if (pos >= 0 && pos < k) {
-      idx_out[pos] = idxs[e];
+      put_index(idx_out, pos, idxs[e], expand);
       sel_out[pos] = sel_value(key, mha, lse0);
     }
     gb += __popc(bg);
@@ -271,7 +282,7 @@ __device__ void emit_lists(Smem<WARPS, WCAP>& sm, uint32_t T, uint32_t k_rem, in
 template <int WARPS, int WCAP, int G, bool CG>
 __device__ void emit_global(const GlobalKeys<G, CG>& src, Smem<WARPS, WCAP>& sm, uint32_t T,
                             uint32_t k_rem, int k, int32_t* idx_out, float* sel_out, bool mha,
-                            float lse0) {
+                            float lse0, int expand) {
   constexpr int kTile = WARPS * 32 * kPer;
   uint32_t cgt = 0, ceq = 0;
   for (int t0 = 0; t0 < src.span; t0 += kTile) {
@@ -302,7 +313,7 @@ __device__ void emit_global(const GlobalKeys<G, CG>& src, Smem<WARPS, WCAP>& sm,
         ++eb;
       }
       if (pos >= 0 && pos < k) {
-        idx_out[pos] = j0 + e;
+        put_index(idx_out, pos, j0 + e, expand);
         sel_out[pos] = sel_value(key[e], mha, lse0);
       }
     }
@@ -339,11 +350,12 @@ __device__ void merge_lse(const float2* part, int u, int b, int hk, int Hq, int 
 }
 
 // The whole selection of one unit, with sm.lse already set and visible to
-// the selecting threads: k positions of [0, span) into idx_u (ascending) and
-// their selection scores into sel_u.
+// the selecting threads: k positions of [0, span) into idx_u (ascending;
+// each expanded to `expand` consecutive rows, see put_index) and their
+// selection scores into sel_u.
 template <int G, bool CG, int WARPS, int WCAP>
 __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int span, int k,
-                            int32_t* idx_u, float* sel_u) {
+                            int32_t* idx_u, float* sel_u, int expand = 1) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) sm.overflow = 0;
   for (int i = threadIdx.x; i < 2048; i += WARPS * 32) sm.hist[i] = 0;
@@ -446,7 +458,7 @@ __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int
     T = (pre << 10) | sm.res[0];
     k_rem -= sm.res[1];
     sync<WARPS>();
-    emit_lists(sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
+    emit_lists(sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0], expand);
   } else {
     // A warp list overflowed: resolve the remaining bits and emit from global memory.
     histogram_global(src, sm, 10, 11, b1);
@@ -459,7 +471,7 @@ __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int
     T = (pre << 10) | sm.res[0];
     k_rem -= sm.res[1];
     sync<WARPS>();
-    emit_global(src, sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0]);
+    emit_global(src, sm, T, k_rem, k, idx_u, sel_u, G == 1, sm.lse[0], expand);
   }
 }
 

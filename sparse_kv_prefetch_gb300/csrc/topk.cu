@@ -21,36 +21,36 @@ __global__ void __launch_bounds__(kTkThreads)
     topk_kernel(const float* __restrict__ logits, const float2* __restrict__ part,
                 int32_t* __restrict__ idx_out, float* __restrict__ sel_out,
                 float* __restrict__ lse_out, int Hq, int Hkv, int ldn, int span, int k,
-                int nchunks) {
+                int nchunks, int expand) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   TkSmem& sm = *reinterpret_cast<TkSmem*>(smem_raw);
   const int u = blockIdx.x, b = u / Hkv, hk = u - b * Hkv;
   sel::merge_lse<G, false>(part, u, b, hk, Hq, nchunks, lse_out, sm);
   sel::sync<kTkWarps>();
   sel::select_unit<G, false>(sm, logits + (size_t)(b * Hq + hk * G) * ldn, ldn, span, k,
-                             idx_out + (size_t)u * k, sel_out + (size_t)u * k);
+                             idx_out + (size_t)u * k * expand, sel_out + (size_t)u * k, expand);
 }
 
 template <int G>
 cudaError_t launch_typed(const Dims& d, const float* logits, const float2* part, int32_t* idx,
-                         float* sel, float* lse, cudaStream_t st) {
+                         float* sel, float* lse, int expand, cudaStream_t st) {
   static unsigned long long prepared = 0;
   cudaError_t e = prepare_kernel(topk_kernel<G>, &prepared, (int)sizeof(TkSmem));
   if (e != cudaSuccess) return e;
-  topk_kernel<G><<<d.U, kTkThreads, sizeof(TkSmem), st>>>(logits, part, idx, sel, lse, d.Hq,
-                                                          d.Hkv, d.ldn, d.span, d.k, d.nchunks);
+  topk_kernel<G><<<d.U, kTkThreads, sizeof(TkSmem), st>>>(
+      logits, part, idx, sel, lse, d.Hq, d.Hkv, d.ldn, d.span, d.k, d.nchunks, expand);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_topk(const Dims& d, const float* logits, const float2* part, int32_t* idx,
-                        float* sel, float* lse, cudaStream_t st) {
+                        float* sel, float* lse, cudaStream_t st, int expand) {
   switch (d.G) {
-    case 1: return launch_typed<1>(d, logits, part, idx, sel, lse, st);
-    case 2: return launch_typed<2>(d, logits, part, idx, sel, lse, st);
-    case 4: return launch_typed<4>(d, logits, part, idx, sel, lse, st);
-    case 8: return launch_typed<8>(d, logits, part, idx, sel, lse, st);
+    case 1: return launch_typed<1>(d, logits, part, idx, sel, lse, expand, st);
+    case 2: return launch_typed<2>(d, logits, part, idx, sel, lse, expand, st);
+    case 4: return launch_typed<4>(d, logits, part, idx, sel, lse, expand, st);
+    case 8: return launch_typed<8>(d, logits, part, idx, sel, lse, expand, st);
   }
   return cudaErrorInvalidValue;
 }
