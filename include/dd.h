@@ -39,7 +39,9 @@
  *  - Supported: head_dim 64 or 128 (fp32) and 64, 128 or 256 (bf16);
  *    H_q % H_kv == 0; 1 <= k <= n - W; 0 <= W < n.  Other shapes return
  *    DD_ERR_UNSUPPORTED or DD_ERR_INVALID_ARG.
- *  - Device pointers must be 16-byte aligned; host KV pointers must come from
+ *  - Device pointers must be 16-byte aligned and belong to the current CUDA
+ *    device (for dd_decode_step, the device the context was created on; the
+ *    call is rejected on any other); host KV pointers must come from
  *    cudaHostAlloc / cudaMallocHost / cudaHostRegister (page-locked, mapped
  *    under unified addressing); pageable host memory is rejected.
  *  - Ownership: the caller owns every buffer passed in; the library never

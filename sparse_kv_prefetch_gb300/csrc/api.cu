@@ -171,13 +171,16 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 dd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DD_OK : DD_ERR_CUDA; }
 
 // True if p is device (or managed) memory of the current CUDA context.
+// Device memory of the current device (or managed memory).
 bool is_device_ptr(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
     cudaGetLastError();
     return false;
   }
-  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
+  if (a.type == cudaMemoryTypeManaged) return true;
+  int dev = -1;
+  return a.type == cudaMemoryTypeDevice && cudaGetDevice(&dev) == cudaSuccess && a.device == dev;
 }
 
 bool all_device(std::initializer_list<const void*> ps) {
@@ -710,13 +713,18 @@ dd_status dd_ctx_set_landmark_chunk(dd_ctx* c, int chunk) {
       cudaGetLastError();
       return DD_ERR_OOM;
     }
-    if (cudaMemset(static_cast<char*>(c->lm_ws) + L.lay.counters, 0,
-                   (size_t)L.lm.U * sizeof(int32_t)) != cudaSuccess ||
-        cudaDeviceSynchronize() != cudaSuccess)
-      return DD_ERR_CUDA;
     c->device_bytes += L.total;
   } else {
     L.total = have;  // keep the larger buffer's size on record
+    cudaDeviceSynchronize();  // a step may still use the buffer in its old layout
+  }
+  // The fused selection's counters of this layout start at zero (in a reused
+  // buffer that memory held something else).
+  if (cudaMemset(static_cast<char*>(c->lm_ws) + L.lay.counters, 0,
+                 (size_t)L.lm.U * sizeof(int32_t)) != cudaSuccess ||
+      cudaDeviceSynchronize() != cudaSuccess) {
+    c->lm_chunk = 0;
+    return DD_ERR_CUDA;
   }
   c->lm = L;
   c->lm_chunk = chunk;
@@ -726,6 +734,8 @@ dd_status dd_ctx_set_landmark_chunk(dd_ctx* c, int chunk) {
 dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
                          dd_stream_t compute, dd_stream_t copy, int flags) {
   if (!c || !layers || n_layers < 1) return DD_ERR_INVALID_ARG;
+  int cur_dev = -1;
+  if (cudaGetDevice(&cur_dev) != cudaSuccess || cur_dev != c->device) return DD_ERR_INVALID_ARG;
   const Dims& d = c->dims;
   // Synchronous checks of every layer before anything is enqueued.
   std::vector<const void*> kh(n_layers), vh(n_layers);
