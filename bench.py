@@ -59,10 +59,11 @@ def parse():
                    help="priority of the copy stream relative to the compute stream")
     p.add_argument("--slots", type=int, default=0,
                    help="override the number of distinct layer slots (memory-limited runs)")
-    p.add_argument("--schedule", default="overlap", choices=["overlap", "late", "pipeline"],
+    p.add_argument("--schedule", default="overlap",
+                   choices=["overlap", "late", "pipeline", "serial"],
                    help="overlap: gather l+1 beside attention l; late: gather l+1 after "
                         "attention l; pipeline: gather and attention of each layer on the "
-                        "copy stream")
+                        "copy stream; serial: every phase in order on one stream")
     p.add_argument("--correct-misses", action="store_true",
                    help="correct prediction misses in every timed layer (DD_STEP_CORRECT_MISSES)")
     p.add_argument("--landmarks", type=int, default=0, metavar="C",
@@ -309,6 +310,7 @@ def run_ours(args, rank, world):
         compute, copy = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
     else:
         compute, copy = torch.cuda.Stream(priority=-1), torch.cuda.Stream()
+    sched_copy = None if args.schedule == "serial" else copy  # None: one stream
     C = args.landmarks
     lm_d = None
     if C:  # chunk landmarks of every layer slot, built once (prefill-time work)
@@ -457,7 +459,7 @@ def run_ours(args, rank, world):
 
     compute.wait_stream(torch.cuda.current_stream())
     for _ in range(max(3, args.warmup)):
-        step(copy)
+        step(sched_copy)
     torch.cuda.synchronize()
     n_serial = max(3, args.steps // 4)
     n_phase = max(3, args.steps // 2)
@@ -471,7 +473,7 @@ def run_ours(args, rank, world):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev0.record(compute)
     for _ in range(args.steps):
-        step(copy, timing="light")  # events around the scoring phase only
+        step(sched_copy, timing="light")  # events around the scoring phase only
     ev1.record(compute)
     torch.cuda.synchronize()
     barrier(world)
@@ -484,7 +486,7 @@ def run_ours(args, rank, world):
     ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev2.record(compute)
     for _ in range(args.steps):
-        step(copy, timing=False)
+        step(sched_copy, timing=False)
     ev3.record(compute)
     torch.cuda.synchronize()
     bare_s = max_over_ranks(ev2.elapsed_time(ev3) * 1e-3, world)
@@ -492,7 +494,7 @@ def run_ours(args, rank, world):
 
     # Phase breakdown: the same steps with events around every phase.
     for _ in range(n_phase):
-        step(copy)
+        step(sched_copy)
     torch.cuda.synchronize()
     phases, _ = recorded(n_phase)
     total_s = ev0.elapsed_time(ev1) * 1e-3
@@ -519,7 +521,8 @@ def run_ours(args, rank, world):
         with torch.cuda.stream(compute):
             qs_l.copy_(qs_src, non_blocking=True)
             q_l.copy_(q_src, non_blocking=True)
-        ctx.decode_step(layers_e2e, compute=compute, copy=copy, late_gather=late, pipeline=pipe,
+        ctx.decode_step(layers_e2e, compute=compute, copy=sched_copy, late_gather=late,
+                        pipeline=pipe,
                         gather_mode=args.gather_mode, correct_misses=args.correct_misses,
                         landmarks=bool(C), fused_topk=args.fused_topk)
         with torch.cuda.stream(compute):

@@ -261,3 +261,30 @@ def test_landmark_full_size_sampled_units(name):
     ctx.close()
     del s, lmk, outs
     _free()
+
+
+def test_chunk_change_reuses_workspace_and_fused_selection_still_agrees():
+    """Setting a smaller chunk after a larger one reuses the context's landmark
+    workspace in a new layout; the fused selection (which keeps per-unit
+    counters in that workspace) and the two-kernel one still agree."""
+    w = C2.scaled(batch=1, n_q_heads=4, n_kv_heads=2, ctx_len=4160, top_k=64, window=64)
+    s = Slot(w)
+    L = 2
+    ctx = dd.Ctx(dd_shape(w))
+    ctx.set_landmark_chunk(8)  # M = 512: the larger workspace
+    lm8 = Landmarks(w, s, 8)
+    outs = [torch.empty((w.batch, w.n_q_heads, w.head_dim), device="cuda") for _ in range(L)]
+    ctx.decode_step(_layers(w, [s], outs, [lm8], L), landmarks=True, fused_topk=True)
+    ctx.set_landmark_chunk(16)  # M = 256: reuses it
+    lm16 = Landmarks(w, s, 16)
+    runs = []
+    for fused in (True, False, True):
+        o = [torch.full_like(outs[0], float("nan")) for _ in range(L)]
+        ctx.decode_step(_layers(w, [s], o, [lm16], L), landmarks=True, fused_topk=fused)
+        runs.append(o)
+    torch.cuda.synchronize()
+    for r in runs[1:]:
+        for l in range(L):
+            assert torch.equal(r[l], runs[0][l])
+    dd.check_device()
+    ctx.close()

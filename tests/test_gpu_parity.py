@@ -227,6 +227,26 @@ def test_fused_selection_equals_two_kernels(name):
     ctx.close()
 
 
+@pytest.mark.parametrize("name", ["c2_mini", "f32_d128", "gqa8_d256"])
+def test_window_keys_from_their_own_buffer(name):
+    """The window's keys read from a separate [B][H_kv][W][d] buffer (k_win)
+    give the same outputs as reading them from the key cache."""
+    w = SMALL[name]
+    s = Slot(w)
+    L = 2
+    k_win = s.K[:, :, w.ctx_len - w.window:, :].contiguous()
+    ctx = dd.Ctx(dd_shape(w))
+    a = [torch.full((w.batch, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
+         for _ in range(L)]
+    b = [torch.full_like(a[0], float("nan")) for _ in range(L)]
+    ctx.decode_step(_layers(w, [s], a, L))
+    ctx.decode_step([io._replace(k_win=k_win) for io in _layers(w, [s], b, L)])
+    torch.cuda.synchronize()
+    for l in range(L):
+        assert torch.equal(a[l], b[l])
+    ctx.close()
+
+
 def test_timing_ring_keeps_back_to_back_steps():
     """With a timing depth of 3, three timed steps enqueued back to back are
     all readable afterwards; a fourth step pushes the oldest out."""
