@@ -181,12 +181,15 @@ __global__ void __launch_bounds__(kScoreThreads)
       for (int i = 0; i < RPG; ++i) {
         float kf[VEC];
         unpack(st[(size_t)(i * NG + grp) * LPR + sub], kf);
+        // Packed fp32 FMA (two lanes of arithmetic per instruction): the even
+        // and the odd elements accumulate separately and are added at the end.
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float a = 0.f;
+          float2 a = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) a = fmaf(qf[g][e], kf[e], a);
-          acc[g * RPG + i] = a;
+          for (int e = 0; e < VEC; e += 2)
+            a = __ffma2_rn(make_float2(qf[g][e], qf[g][e + 1]), make_float2(kf[e], kf[e + 1]), a);
+          acc[g * RPG + i] = a.x + a.y;
         }
       }
       __syncwarp();
