@@ -132,10 +132,12 @@ dd_status dd_host_free(void* p);
 size_t dd_host_page_bytes(void);
 
 /*
- * Bytes of device workspace that dd_score_topk and dd_sparse_decode_attn need
- * for this shape (fp32 logits [B][H_q][round_up(n,4)], per-chunk softmax
- * partials and split-k attention partials, each 256-byte aligned).
- * The two calls use disjoint parts, so one buffer serves both.
+ * Bytes of device workspace that dd_score_topk, dd_sparse_decode_attn and
+ * dd_correct_misses need for this shape (fp32 logits [B][H_q][round_up(n,4)],
+ * per-chunk softmax partials, split-k attention partials, the real query's
+ * selection scores and B*H_kv counters of the fused selection, each region
+ * 256-byte aligned).  The calls use disjoint parts, so one buffer serves them
+ * all (but two calls in flight at once need two buffers).
  * Returns DD_ERR_INVALID_ARG / DD_ERR_UNSUPPORTED for bad shapes.
  */
 dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes);
