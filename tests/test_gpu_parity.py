@@ -147,6 +147,14 @@ def test_exact_ties_take_lowest_positions(n):
         np.testing.assert_allclose(lse[0, u], np.log(n), atol=1e-3)
         np.testing.assert_allclose(sel[u], 1.0 / n, rtol=2e-3)
         check_unit_attention(w, s, u, idx[u], o.out.cpu().numpy())
+    # The fused selection (8 warps of 1024 entries: n = 20000 overflows it too)
+    # picks the same rows, so the layer loop reproduces the output bit for bit.
+    ctx = dd.Ctx(dd_shape(w))
+    out = torch.full_like(o.out, float("nan"))
+    ctx.decode_step(_layers(w, [s], [out], 1), fused_topk=True)
+    torch.cuda.synchronize()
+    assert torch.equal(out, o.out)
+    ctx.close()
 
 
 def _layers(w, slots, outs, L):
