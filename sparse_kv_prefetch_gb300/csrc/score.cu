@@ -6,15 +6,17 @@
 // being processed and the key cache.)
 //
 // The kernel is HBM-bound: every K row is read exactly once, 2 flops per
-// element.  Each CTA owns one chunk of positions of one (request, KV head)
-// unit.  One producer warp streams the chunk through a ring of shared-memory
-// stages with bulk copies (cp.async.bulk on the tensor-memory-access unit,
-// completion on an mbarrier), so many bytes are in flight per SM without
-// occupying the load/store pipeline or registers.  Eight consumer warps read
-// each stage: LPR lanes share one K row (16 bytes each), the partial dot
-// products are reduced with xor-shuffles, and the lane that owns a row
-// writes its logit and folds it into a running (max, sum of exp).  All query
-// heads of a GQA group are scored from the same K row.
+// element and query head.  Each CTA owns one chunk of positions of one
+// (request, KV head) unit.  One producer warp streams the chunk through a
+// ring of shared-memory stages with bulk copies (cp.async.bulk on the
+// tensor-memory-access unit, completion on an mbarrier, K tagged L2
+// evict-first), so many bytes are in flight per SM without occupying the
+// load/store pipeline or registers.  Eight consumer warps read each stage:
+// LPR lanes share one K row (16 bytes each), the dot products use packed fp32
+// FMAs, the partial sums are reduced with a transposed xor-shuffle butterfly,
+// and the lane that owns a row writes its logit and folds it into a running
+// (max, sum of exp).  All query heads of a GQA group are scored from the same
+// K row.  With FUSED, the unit's last CTA also runs its top-k (select.cuh).
 #include <math.h>
 
 #include "dd_internal.cuh"
