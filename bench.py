@@ -59,11 +59,14 @@ def parse():
                    help="priority of the copy stream relative to the compute stream")
     p.add_argument("--slots", type=int, default=0,
                    help="override the number of distinct layer slots (memory-limited runs)")
-    p.add_argument("--schedule", default="overlap",
-                   choices=["overlap", "late", "pipeline", "serial"],
+    p.add_argument("--schedule", default="auto",
+                   choices=["auto", "overlap", "late", "pipeline", "serial"],
                    help="overlap: gather l+1 beside attention l; late: gather l+1 after "
                         "attention l; pipeline: gather and attention of each layer on the "
-                        "copy stream; serial: every phase in order on one stream")
+                        "copy stream; serial: every phase in order on one stream; auto: "
+                        "overlap or serial, whichever a short calibration after the warm-up "
+                        "measures faster (scoring and the host gather slow each other when "
+                        "they run together, by an amount that varies between hosts)")
     p.add_argument("--correct-misses", action="store_true",
                    help="correct prediction misses in every timed layer (DD_STEP_CORRECT_MISSES)")
     p.add_argument("--landmarks", type=int, default=0, metavar="C",
@@ -236,7 +239,8 @@ def config_of(w, args):
                   % (w.k_bytes() / 2**20),
             "parallelism": f"replicas x{args.gpus} (independent requests per GPU)",
             "gather_mode": ["bulk_copy", "load_store"][args.gather_mode],
-            "host_store": args.host_alloc, "schedule": args.schedule,
+            "host_store": args.host_alloc,
+            "schedule": getattr(args, "schedule_chosen", args.schedule),
             "copy_stream_priority": args.copy_priority,
             "correct_misses": bool(args.correct_misses),
             "landmark_chunk": args.landmarks or None,
@@ -461,6 +465,28 @@ def run_ours(args, rank, world):
     for _ in range(max(3, args.warmup)):
         step(sched_copy)
     torch.cuda.synchronize()
+    if args.schedule == "auto":
+        # Calibration: overlap and serial alternately, 3 untimed-inside steps each, twice.
+        cal = {"overlap": 0.0, "serial": 0.0}
+        for _ in range(2):
+            for name, cs in (("overlap", copy), ("serial", None)):
+                c0 = torch.cuda.Event(enable_timing=True)
+                c1 = torch.cuda.Event(enable_timing=True)
+                c0.record(compute)
+                for _ in range(3):
+                    step(cs, timing=False)
+                c1.record(compute)
+                torch.cuda.synchronize()
+                cal[name] += c0.elapsed_time(c1) / 6
+        pick = min(cal, key=cal.get)
+        if world > 1:  # every rank runs the same schedule: rank 0's choice
+            import torch.distributed as dist
+            t = torch.tensor([0 if pick == "overlap" else 1], device=dev)
+            dist.broadcast(t, 0)
+            pick = "overlap" if int(t) == 0 else "serial"
+        sched_copy = copy if pick == "overlap" else None
+        args.schedule_chosen = (f"{pick} (auto; calibration ms per step: overlap "
+                                f"{cal['overlap']:.2f}, serial {cal['serial']:.2f})")
     n_serial = max(3, args.steps // 4)
     n_phase = max(3, args.steps // 2)
     ctx.set_timing_depth(max(args.steps, n_serial, n_phase))
