@@ -518,6 +518,21 @@ def run_ours(args, rank, world):
     bare_s = max_over_ranks(ev2.elapsed_time(ev3) * 1e-3, world)
     value_bare = job_throughput(L, args.steps, bare_s, world)
 
+    # The same steps as one CUDA graph launch each (captured once).
+    ctx.capture_step(layers, compute, copy=sched_copy, late_gather=late, pipeline=pipe,
+                     gather_mode=args.gather_mode, correct_misses=args.correct_misses,
+                     landmarks=bool(C), fused_topk=args.fused_topk)
+    ctx.replay_step(compute)
+    torch.cuda.synchronize()
+    ev4, ev5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev4.record(compute)
+    for _ in range(args.steps):
+        ctx.replay_step(compute)
+    ev5.record(compute)
+    torch.cuda.synchronize()
+    value_graph = job_throughput(L, args.steps,
+                                 max_over_ranks(ev4.elapsed_time(ev5) * 1e-3, world), world)
+
     # Phase breakdown: the same steps with events around every phase.
     for _ in range(n_phase):
         step(sched_copy)
@@ -619,6 +634,9 @@ def run_ours(args, rank, world):
         "value_without_layer_events": value_bare,
         "value_without_layer_events_what": "the same K steps right after the timed region, "
                                            "with no events inside the steps",
+        "value_graph": value_graph,
+        "value_graph_what": "the same K steps, each one launch of the step captured as a "
+                            "CUDA graph (dd_ctx_capture_step / dd_ctx_replay_step)",
         "serial_phase_ms_per_step": {kk: statistics.mean(p[kk] for p in serial)
                                      for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms",
                                                 "attn_ms")},

@@ -380,6 +380,22 @@ dd_status dd_ctx_set_landmark_chunk(dd_ctx* ctx, int chunk);
 dd_status dd_decode_step(dd_ctx* ctx, const dd_layer_io* layers, int n_layers,
                          dd_stream_t compute, dd_stream_t copy, int flags);
 
+/*
+ * Capture one decode step (same arguments as dd_decode_step, without the
+ * timing flags) into a CUDA graph held by the context, replacing any earlier
+ * one.  The step is first run once directly on `compute` (and synchronised),
+ * so that everything it allocates lazily exists, then captured from
+ * `compute` (the copy stream joins the capture through the step's events).
+ * The graph keeps the layer pointers it was captured with: capture again when
+ * they change.  DD_ERR_UNSUPPORTED with timing flags.
+ */
+dd_status dd_ctx_capture_step(dd_ctx* ctx, const dd_layer_io* layers, int n_layers,
+                              dd_stream_t compute, dd_stream_t copy, int flags);
+
+/* Launch the captured step on `stream` (one graph launch: the whole step,
+ * both streams' work, with the same ordering as dd_decode_step). */
+dd_status dd_ctx_replay_step(dd_ctx* ctx, dd_stream_t stream);
+
 /* Phase times of the last dd_decode_step run with DD_STEP_TIMING, in ms. */
 typedef struct {
   float step_ms;      /* first event to last event on `compute` */

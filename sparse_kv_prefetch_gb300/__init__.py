@@ -117,6 +117,9 @@ def _lib():
                                         ctypes.c_int),
             "dd_ctx_set_landmark_chunk": ([P, ctypes.c_int], ctypes.c_int),
             "dd_ctx_set_timing_depth": ([P, ctypes.c_int], ctypes.c_int),
+            "dd_ctx_capture_step": ([P, ctypes.POINTER(dd_layer_io), ctypes.c_int, P, P,
+                                     ctypes.c_int], ctypes.c_int),
+            "dd_ctx_replay_step": ([P, P], ctypes.c_int),
             "dd_ctx_step_timings": ([P, ctypes.c_int, ctypes.POINTER(dd_phase_times)],
                                     ctypes.c_int),
             "dd_ctx_step_score_times": ([P, ctypes.c_int, ctypes.POINTER(ctypes.c_float),
@@ -356,15 +359,34 @@ class Ctx:
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
         # timing: False, True (every phase) or "light" (step and scoring only)
-        flags = ((DD_STEP_TIMING_LIGHT if timing == "light" else DD_STEP_TIMING if timing else 0)
-                 | (DD_STEP_LATE_GATHER if late_gather else 0)
-                 | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
-                 | (DD_STEP_PIPELINE if pipeline else 0)
-                 | (DD_STEP_CORRECT_MISSES if correct_misses else 0)
-                 | (DD_STEP_LANDMARKS if landmarks else 0)
-                 | (DD_STEP_FUSED_TOPK if fused_topk else 0))
+        flags = self._flags(late_gather, gather_mode, pipeline, correct_misses, landmarks,
+                            fused_topk, timing)
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
+
+    @staticmethod
+    def _flags(late_gather=False, gather_mode=0, pipeline=False, correct_misses=False,
+               landmarks=False, fused_topk=False, timing=False):
+        return ((DD_STEP_TIMING_LIGHT if timing == "light" else DD_STEP_TIMING if timing else 0)
+                | (DD_STEP_LATE_GATHER if late_gather else 0)
+                | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
+                | (DD_STEP_PIPELINE if pipeline else 0)
+                | (DD_STEP_CORRECT_MISSES if correct_misses else 0)
+                | (DD_STEP_LANDMARKS if landmarks else 0)
+                | (DD_STEP_FUSED_TOPK if fused_topk else 0))
+
+    def capture_step(self, layers, compute, copy=None, **schedule):
+        """Capture one decode step into a CUDA graph held by the context (the
+        step runs once directly first); replay it with replay_step."""
+        arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
+        _check(_lib().dd_ctx_capture_step(self._h, arr, len(arr), _stream(compute),
+                                          None if copy is None else _stream(copy),
+                                          self._flags(**schedule)), "dd_ctx_capture_step")
+        self._keep_graph = arr
+
+    def replay_step(self, stream=None):
+        """Launch the captured step (one graph launch)."""
+        _check(_lib().dd_ctx_replay_step(self._h, _stream(stream)), "dd_ctx_replay_step")
 
     def set_timing_depth(self, depth: int):
         """Keep the events of the last `depth` timed steps (read with back=...)."""

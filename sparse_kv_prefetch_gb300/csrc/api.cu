@@ -549,6 +549,10 @@ struct dd_ctx {
   LandmarkDims lm;
   void* lm_ws;  // its own workspace: under DD_STEP_PIPELINE the selection of
                 // layer l+1 runs beside the attention of layer l
+  // A captured decode step (dd_ctx_capture_step), replayed by dd_ctx_replay_step.
+  cudaGraph_t graph;
+  cudaGraphExec_t graph_exec;
+  int graph_launches;
 };
 
 namespace {
@@ -558,6 +562,8 @@ void ctx_free(dd_ctx* c) {
   int prev = -1;
   cudaGetDevice(&prev);
   cudaSetDevice(c->device);
+  if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+  if (c->graph) cudaGraphDestroy(c->graph);
   for (int i = 0; i < 2; ++i) {
     cudaFree(c->kbuf[i]);
     cudaFree(c->vbuf[i]);
@@ -840,8 +846,14 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     if (!serial) {
       e = cudaStreamWaitEvent(X, c->ev_idx[s], 0);
       if (e != cudaSuccess) return e;
-      e = cudaStreamWaitEvent(X, c->ev_free[s], 0);
-      if (e != cudaSuccess) return e;
+      // The slot's last reader is the attention of layer l - 2 of this step.
+      // For l < 2 it belongs to an earlier step, which the copy stream is
+      // already ordered after (it waited for all earlier compute work at the
+      // start of this step); a wait on that event could not be captured.
+      if (l >= 2) {
+        e = cudaStreamWaitEvent(X, c->ev_free[s], 0);
+        if (e != cudaSuccess) return e;
+      }
     }
     if (phases) cudaEventRecord(T(l, PH_GATHER0), X);
     e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X);
@@ -946,6 +958,56 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   }
 #undef DD_TRY
   return DD_OK;
+}
+
+dd_status dd_ctx_capture_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
+                              dd_stream_t compute, dd_stream_t copy, int flags) {
+  if (!c || !layers || n_layers < 1 || !compute) return DD_ERR_INVALID_ARG;
+  if (flags & (DD_STEP_TIMING | DD_STEP_TIMING_LIGHT)) return DD_ERR_UNSUPPORTED;
+  int cur_dev = -1;
+  if (cudaGetDevice(&cur_dev) != cudaSuccess || cur_dev != c->device) return DD_ERR_INVALID_ARG;
+  cudaStream_t C = reinterpret_cast<cudaStream_t>(compute);
+  // Per-layer buffers that a step allocates on first use must exist before
+  // capture (allocation is not captured): run the checks and the lazy
+  // allocations outside it, through a step on the caller's stream that is
+  // synchronised before capturing.
+  dd_status st = dd_decode_step(c, layers, n_layers, compute, copy, flags);
+  if (st != DD_OK) return st;
+  if (cudaStreamSynchronize(C) != cudaSuccess) return DD_ERR_CUDA;
+  if (c->graph_exec) cudaGraphExecDestroy(c->graph_exec);
+  if (c->graph) cudaGraphDestroy(c->graph);
+  c->graph_exec = nullptr;
+  c->graph = nullptr;
+  c->graph_launches = 0;
+  if (cudaStreamBeginCapture(C, cudaStreamCaptureModeThreadLocal) != cudaSuccess)
+    return DD_ERR_CUDA;
+  st = dd_decode_step(c, layers, n_layers, compute, copy, flags);
+  cudaGraph_t g = nullptr;
+  const cudaError_t e = cudaStreamEndCapture(C, &g);
+  if (st != DD_OK || e != cudaSuccess || !g) {
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();
+    return st != DD_OK ? st : DD_ERR_CUDA;
+  }
+  cudaGraphExec_t x = nullptr;
+  if (cudaGraphInstantiate(&x, g, 0) != cudaSuccess) {
+    cudaGraphDestroy(g);
+    cudaGetLastError();
+    return DD_ERR_CUDA;
+  }
+  size_t n_nodes = 0;
+  cudaGraphGetNodes(g, nullptr, &n_nodes);
+  c->graph = g;
+  c->graph_exec = x;
+  c->graph_launches = (int)n_nodes;
+  return DD_OK;
+}
+
+dd_status dd_ctx_replay_step(dd_ctx* c, dd_stream_t stream) {
+  if (!c || !c->graph_exec) return DD_ERR_INVALID_ARG;
+  int cur_dev = -1;
+  if (cudaGetDevice(&cur_dev) != cudaSuccess || cur_dev != c->device) return DD_ERR_INVALID_ARG;
+  return cuda_status(cudaGraphLaunch(c->graph_exec, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dd_status dd_ctx_step_timings(dd_ctx* c, int back, dd_phase_times* out) {

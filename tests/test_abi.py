@@ -130,6 +130,8 @@ def test_timing_calls_reject_null_context():
     assert lib.dd_ctx_set_timing_depth(None, 4) == dd.DD_ERR_INVALID_ARG
     assert lib.dd_ctx_step_timings(None, 0, ctypes.byref(t)) == dd.DD_ERR_INVALID_ARG
     assert lib.dd_ctx_timings(None, ctypes.byref(t)) == dd.DD_ERR_INVALID_ARG
+    assert lib.dd_ctx_capture_step(None, None, 1, None, None, 0) == dd.DD_ERR_INVALID_ARG
+    assert lib.dd_ctx_replay_step(None, None) == dd.DD_ERR_INVALID_ARG
 
 
 def test_pageable_host_store_rejected_by_binding():

@@ -255,6 +255,38 @@ def test_window_keys_from_their_own_buffer(name):
     ctx.close()
 
 
+@pytest.mark.parametrize("name", ["c1", "c2_mini", "c5_mini"])
+def test_captured_step_replays_bit_identical(name):
+    """A decode step captured into a CUDA graph and replayed (several times,
+    in each schedule) writes the same outputs as the direct step."""
+    w = SMALL[name]
+    D, L = 2, 4
+    slots = [Slot(w, d) for d in range(D)]
+    ctx = dd.Ctx(dd_shape(w))
+    compute = torch.cuda.Stream()
+    copy = torch.cuda.Stream(priority=-1)
+    compute.wait_stream(torch.cuda.current_stream())
+    ref = [torch.empty((w.batch, w.n_q_heads, w.head_dim), device="cuda") for _ in range(L)]
+    ctx.decode_step(_layers(w, slots, ref, L), compute=compute, copy=copy)
+    for sched in (dict(copy=copy), dict(copy=None), dict(copy=copy, pipeline=True),
+                  dict(copy=copy, fused_topk=True)):
+        outs = [torch.full_like(ref[0], float("nan")) for _ in range(L)]
+        layers = dd.Ctx.pack(_layers(w, slots, outs, L))
+        ctx.capture_step(layers, compute, **sched)
+        for o in outs:
+            o.fill_(float("nan"))
+        compute.synchronize()
+        for _ in range(3):
+            ctx.replay_step(compute)
+        compute.synchronize()
+        for l in range(L):
+            assert torch.equal(outs[l], ref[l]), f"{sched}: layer {l}"
+    with pytest.raises(dd.DDError):  # timing is not captured
+        ctx.capture_step(_layers(w, slots, ref, L), compute, copy=copy, timing=True)
+    dd.check_device()
+    ctx.close()
+
+
 def test_timing_ring_keeps_back_to_back_steps():
     """With a timing depth of 3, three timed steps enqueued back to back are
     all readable afterwards; a fourth step pushes the oldest out."""
