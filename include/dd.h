@@ -255,6 +255,15 @@ dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_
                             int32_t* miss_out, float* mass_out, void* workspace, size_t ws_bytes,
                             dd_stream_t stream);
 
+/*
+ * Test hook (no counterpart in the paper): enqueue on `stream` a wait that
+ * nothing completes; it gives up after limit_ns (1 ns .. 100 ms) through the
+ * same bounded-wait path every kernel of the library uses, and the next
+ * dd_check_device returns DD_ERR_TIMEOUT.  The kernel returns normally, so
+ * the context stays usable.
+ */
+dd_status dd_debug_expire_wait(uint64_t limit_ns, dd_stream_t stream);
+
 /* ------------------------ landmark selection ------------------------ */
 
 /*
@@ -354,6 +363,10 @@ enum {
                               (no separate top-k launch; same results).  Off by
                               default: on GB300 the two-kernel form measured
                               faster on the MHA and GQA workloads */
+  DD_STEP_DEBUG_DELAY_COPY = 512,     /* test hook: a 50 us GPU sleep before each
+                                         gather, on the stream that runs it */
+  DD_STEP_DEBUG_DELAY_COMPUTE = 1024, /* test hook: the same before each attention;
+                                         with either, results must not change */
   DD_STEP_LANDMARKS = 32   /* select with dd_score_topk_landmarks over each
                               layer's `landmarks` instead of scoring every key
                               (chunk set by dd_ctx_set_landmark_chunk; not

@@ -30,6 +30,8 @@ DD_STEP_CORRECT_MISSES = 16
 DD_STEP_LANDMARKS = 32
 DD_STEP_TIMING_LIGHT = 64
 DD_STEP_FUSED_TOPK = 128
+DD_STEP_DEBUG_DELAY_COPY = 512
+DD_STEP_DEBUG_DELAY_COMPUTE = 1024
 
 
 class DDError(RuntimeError):
@@ -120,6 +122,7 @@ def _lib():
             "dd_ctx_capture_step": ([P, ctypes.POINTER(dd_layer_io), ctypes.c_int, P, P,
                                      ctypes.c_int], ctypes.c_int),
             "dd_ctx_replay_step": ([P, P], ctypes.c_int),
+            "dd_debug_expire_wait": ([ctypes.c_uint64, P], ctypes.c_int),
             "dd_ctx_step_timings": ([P, ctypes.c_int, ctypes.POINTER(dd_phase_times)],
                                     ctypes.c_int),
             "dd_ctx_step_score_times": ([P, ctypes.c_int, ctypes.POINTER(ctypes.c_float),
@@ -199,6 +202,12 @@ def host_empty(shape, dtype):
 
 def host_page_bytes() -> int:
     return _lib().dd_host_page_bytes()
+
+
+def debug_expire_wait(limit_ns: int, stream=None):
+    """Test hook: a device wait that nothing completes gives up after limit_ns;
+    the next check_device raises DD_ERR_TIMEOUT (see dd.h)."""
+    _check(_lib().dd_debug_expire_wait(limit_ns, _stream(stream)), "dd_debug_expire_wait")
 
 
 def check_device():
@@ -353,21 +362,23 @@ class Ctx:
     def decode_step(self, layers, compute=None, copy=None, timing=False,
                     late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False,
                     correct_misses: bool = False, landmarks: bool = False,
-                    fused_topk: bool = False):
+                    fused_topk: bool = False, debug_delay: str = ""):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
         # timing: False, True (every phase) or "light" (step and scoring only)
         flags = self._flags(late_gather, gather_mode, pipeline, correct_misses, landmarks,
-                            fused_topk, timing)
+                            fused_topk, timing, debug_delay)
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 
     @staticmethod
     def _flags(late_gather=False, gather_mode=0, pipeline=False, correct_misses=False,
-               landmarks=False, fused_topk=False, timing=False):
-        return ((DD_STEP_TIMING_LIGHT if timing == "light" else DD_STEP_TIMING if timing else 0)
+               landmarks=False, fused_topk=False, timing=False, debug_delay=""):
+        return ((DD_STEP_DEBUG_DELAY_COPY if "copy" in debug_delay else 0)
+                | (DD_STEP_DEBUG_DELAY_COMPUTE if "compute" in debug_delay else 0)
+                | (DD_STEP_TIMING_LIGHT if timing == "light" else DD_STEP_TIMING if timing else 0)
                 | (DD_STEP_LATE_GATHER if late_gather else 0)
                 | (DD_STEP_GATHER_LSU if gather_mode == 1 else 0)
                 | (DD_STEP_PIPELINE if pipeline else 0)

@@ -19,7 +19,7 @@ OUT = os.path.join(HERE, "libdd.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["api.cu", "score.cu", "topk.cu", "gather.cu", "attn.cu", "correct.cu", "noalloc.cu",
-           "landmark.cu"]
+           "landmark.cu", "debug.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I", INCLUDE, "-I", CSRC]

@@ -294,7 +294,13 @@ dd_status dd_check_device(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return DD_ERR_CUDA;
   const unsigned int a = take_score_status();
   const unsigned int b = take_gather_status();
-  return (a | b) ? DD_ERR_TIMEOUT : DD_OK;
+  const unsigned int c = take_debug_status();
+  return (a | b | c) ? DD_ERR_TIMEOUT : DD_OK;
+}
+
+dd_status dd_debug_expire_wait(uint64_t limit_ns, dd_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 100000000ull) return DD_ERR_INVALID_ARG;
+  return cuda_status(launch_expire_wait(limit_ns, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes) {
@@ -770,6 +776,9 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   const bool correct = (flags & DD_STEP_CORRECT_MISSES) != 0;
   const bool use_lm = (flags & DD_STEP_LANDMARKS) != 0;
   const bool fused = (flags & DD_STEP_FUSED_TOPK) != 0;
+  const bool delay_copy = (flags & DD_STEP_DEBUG_DELAY_COPY) != 0;
+  const bool delay_compute = (flags & DD_STEP_DEBUG_DELAY_COMPUTE) != 0;
+  constexpr uint64_t kDebugDelayNs = 50000;  // 50 us before each gather / attention
   if (use_lm) {
     if (c->lm_chunk == 0 || correct) return DD_ERR_UNSUPPORTED;
     for (int l = 0; l < n_layers; ++l) {
@@ -855,6 +864,10 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
         if (e != cudaSuccess) return e;
       }
     }
+    if (delay_copy) {
+      e = launch_delay(kDebugDelayNs, X);
+      if (e != cudaSuccess) return e;
+    }
     if (phases) cudaEventRecord(T(l, PH_GATHER0), X);
     e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X);
     if (e != cudaSuccess) return e;
@@ -872,6 +885,10 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     cudaError_t e;
     if (!serial && !pipeline) {
       e = cudaStreamWaitEvent(C, c->ev_ready[s], 0);
+      if (e != cudaSuccess) return e;
+    }
+    if (delay_compute) {
+      e = launch_delay(kDebugDelayNs, A);
       if (e != cudaSuccess) return e;
     }
     if (phases) cudaEventRecord(T(l, PH_ATTN0), A);

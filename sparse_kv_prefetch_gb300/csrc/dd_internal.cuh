@@ -142,6 +142,12 @@ int score_chunk(int dtype, int head_dim, long long units, int n);
 // wait gives up (nonzero: some wait timed out since the last read).
 unsigned int take_score_status();
 unsigned int take_gather_status();
+unsigned int take_debug_status();
+
+// Test hooks (debug.cu): a bounded GPU sleep on a stream, and a wait that
+// nothing completes, which gives up after limit_ns and sets the status word.
+cudaError_t launch_delay(uint64_t ns, cudaStream_t st);
+cudaError_t launch_expire_wait(uint64_t limit_ns, cudaStream_t st);
 
 // ----------------------------------------------------------------- device
 
@@ -233,12 +239,15 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Every wait in this library is bounded: after kWaitLimitNs the wait gives up
 // and returns false; the caller records DD_ERR_TIMEOUT and stops its work.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   return true;
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  return mbar_wait_for(bar, parity, kWaitLimitNs);
 }
 // global -> shared, completion counted on `bar` (bytes and addresses 16-aligned).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,

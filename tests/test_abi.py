@@ -132,6 +132,8 @@ def test_timing_calls_reject_null_context():
     assert lib.dd_ctx_timings(None, ctypes.byref(t)) == dd.DD_ERR_INVALID_ARG
     assert lib.dd_ctx_capture_step(None, None, 1, None, None, 0) == dd.DD_ERR_INVALID_ARG
     assert lib.dd_ctx_replay_step(None, None) == dd.DD_ERR_INVALID_ARG
+    assert lib.dd_debug_expire_wait(0, None) == dd.DD_ERR_INVALID_ARG
+    assert lib.dd_debug_expire_wait(200_000_000, None) == dd.DD_ERR_INVALID_ARG
 
 
 def test_pageable_host_store_rejected_by_binding():
