@@ -51,8 +51,9 @@ def parse():
     p.add_argument("--workload", default=synth.C2.name, choices=list(synth.WORKLOADS))
     p.add_argument("--profile-case", action="store_true",
                    help="small case for ncu captures: batch 2, 2 layers, 1 slot")
-    p.add_argument("--gather-mode", type=int, default=0, choices=[0, 1],
-                   help="0: bulk-copy gather, 1: load/store gather")
+    p.add_argument("--gather-mode", type=int, default=None, choices=[0, 1],
+                   help="0: bulk-copy gather, 1: load/store gather (default: 0, or 1 with "
+                        "--landmarks, where whole chunks make it the faster one)")
     p.add_argument("--host-alloc", default="pinned", choices=["huge", "pinned"],
                    help="host KV store: dd_host_alloc huge pages, or torch pinned memory")
     p.add_argument("--copy-priority", default="high", choices=["high", "low"],
@@ -80,6 +81,12 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU work budget of the oracle baseline")
     return p.parse_args()
+
+
+def resolve_defaults(args):
+    if args.gather_mode is None:
+        args.gather_mode = 1 if args.landmarks else 0
+    return args
 
 
 def workload(args):
@@ -671,7 +678,7 @@ def run_ours(args, rank, world):
 
 
 def main():
-    args = parse()
+    args = resolve_defaults(parse())
     rank, world = dist_init(args)
     if args.impl == "reference":
         run_reference(args, rank, world)

@@ -89,17 +89,31 @@ __global__ void __launch_bounds__(32)
   }
   __syncwarp();
 
-  // Issue the row copies of `tile` into stage s.
+  // Issue the row copies of `tile` into stage s.  Rows whose positions are
+  // consecutive (whole chunks under landmark selection) are contiguous in the
+  // host store and in the tile, so each run of them is one bulk copy: the
+  // lane holding the first row of a run copies the run.
   auto issue = [&](int tile, int s) {
     const int u = tile / tiles_per_unit, i0 = (tile - u * tiles_per_unit) * R;
     const int nr = min(R, k - i0);
     if (lane == 0) mbar_arrive_expect_tx(&full[s], (uint32_t)(2 * nr * RB));
     __syncwarp();
-    for (int r = lane; r < nr; r += 32) {
-      const int j = min(max(__ldg(idx + (size_t)u * k + i0 + r), 0), n - 1);  // never outside
-      const size_t src = ((size_t)u * n + j) * RB;
-      bulk_load(ring_k + (size_t)s * kTileBytes + (size_t)r * RB, k_host + src, RB, &full[s]);
-      bulk_load(ring_v + (size_t)s * kTileBytes + (size_t)r * RB, v_host + src, RB, &full[s]);
+    for (int r0 = 0; r0 < nr; r0 += 32) {
+      const int r = r0 + lane;
+      const bool valid = r < nr;
+      int j = 0;
+      if (valid) j = min(max(__ldg(idx + (size_t)u * k + i0 + r), 0), n - 1);  // never outside
+      const int jp = __shfl_up_sync(0xffffffffu, j, 1);
+      const bool cont = valid && lane > 0 && jp + 1 == j;  // continues the run before it
+      const unsigned cmask = __ballot_sync(0xffffffffu, cont);
+      if (valid && !cont) {
+        const unsigned after = lane == 31 ? 0u : cmask >> (lane + 1);
+        const int len = __ffs(~after);  // this row plus the continuing rows after it
+        const size_t src = ((size_t)u * n + j) * RB;
+        const uint32_t bytes = (uint32_t)(len * RB);
+        bulk_load(ring_k + (size_t)s * kTileBytes + (size_t)r * RB, k_host + src, bytes, &full[s]);
+        bulk_load(ring_v + (size_t)s * kTileBytes + (size_t)r * RB, v_host + src, bytes, &full[s]);
+      }
     }
   };
 
