@@ -410,20 +410,28 @@ __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int
       }
       // The kUnroll groups in position order: group v covers
       // [base + v kWarpStep, base + (v + 1) kWarpStep).
+      const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
       for (int v = 0; v < kUnroll; ++v) {
         const int j0 = base + v * kWarpStep + lane * kPer;
         bool f[kPer];
-        uint32_t c = 0;
+        unsigned bal[kPer];
+        unsigned any = 0;
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {
           f[e] = (j0 + e < seg1) && (key[v][e] >> 21) >= b1;
-          c += f[e];
+          bal[e] = __ballot_sync(0xffffffffu, f[e]);
+          any |= bal[e];
         }
-        uint32_t pos = n_w + warp_excl_scan(c, lane);
-        uint32_t tot = c;
+        if (!any) continue;  // most steps: no candidate in the warp
+        // Position order is (lane, e): the entries of the lanes before this
+        // one come first, then this lane's in e order.
+        uint32_t tot = 0, pos = n_w;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+        for (int e = 0; e < kPer; ++e) {
+          tot += __popc(bal[e]);
+          pos += __popc(bal[e] & lt_mask);
+        }
         if (n_w + tot > (uint32_t)WCAP) {
           over = true;  // the same decision in every lane
           break;
