@@ -168,9 +168,9 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
  *                   outside that range is clamped into it on the device, so
  *                   the kernel never reads outside the store
  *   k_buf, v_buf    device [B][H_kv][k][d]
- *   Before the copy, one warp reads a word per huge page of the two host
- *   regions so their address translations are resolved once (a second, tiny
- *   kernel on the same stream).
+ *   If a store was allocated by dd_host_alloc (huge pages), one warp first
+ *   reads a word per huge page of the two host regions so their address
+ *   translations are resolved once (a second, tiny kernel on the same stream).
  *   mode            0 = bulk-copy gather: one-warp CTAs issue one
  *                       cp.async.bulk per row into shared memory and write
  *                       tiles back with bulk stores (used by dd_decode_step);

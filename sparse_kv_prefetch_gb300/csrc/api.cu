@@ -226,6 +226,21 @@ std::mutex g_host_mu;
 std::map<void*, size_t> g_host_regions;  // dd_host_alloc base -> mapped bytes
 }  // namespace
 
+}  // extern "C"
+
+namespace dd {
+bool in_huge_page_store(const void* p) {
+  std::lock_guard<std::mutex> lock(g_host_mu);
+  auto it = g_host_regions.upper_bound(const_cast<void*>(p));
+  if (it == g_host_regions.begin()) return false;
+  --it;
+  const uintptr_t base = (uintptr_t)it->first, q = (uintptr_t)p;
+  return q >= base && q < base + it->second;
+}
+}  // namespace dd
+
+extern "C" {
+
 dd_status dd_host_alloc(size_t bytes, void** out) {
   if (!out || bytes == 0) return DD_ERR_INVALID_ARG;
   *out = nullptr;
@@ -345,8 +360,9 @@ dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v
   const void* vh = host_to_device(v_host);
   if (!kh || !vh) return DD_ERR_INVALID_ARG;
   if (!all_device({idx, k_buf, v_buf})) return DD_ERR_INVALID_ARG;
+  const bool touch = in_huge_page_store(k_host) || in_huge_page_store(v_host);
   return cuda_status(launch_gather(d, kh, vh, idx, k_buf, v_buf, mode,
-                                   reinterpret_cast<cudaStream_t>(stream)));
+                                   reinterpret_cast<cudaStream_t>(stream), touch));
 }
 
 dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void* k_buf,
@@ -751,6 +767,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   const Dims& d = c->dims;
   // Synchronous checks of every layer before anything is enqueued.
   std::vector<const void*> kh(n_layers), vh(n_layers);
+  std::vector<char> touch(n_layers);
   // Without DD_STEP_LANDMARKS the key cache is scored, so k_dev is required;
   // with it, k_dev is needed only for the window's keys, if k_win is NULL.
   const bool lm_flag = (flags & DD_STEP_LANDMARKS) != 0;
@@ -766,6 +783,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     kh[l] = host_to_device(io.k_host);
     vh[l] = host_to_device(io.v_host);
     if (!kh[l] || !vh[l]) return DD_ERR_INVALID_ARG;
+    touch[l] = in_huge_page_store(io.k_host) || in_huge_page_store(io.v_host);
     if (!all_device({io.q_spec, io.q, io.k_dev, io.v_win, io.k_win, io.out}))
       return DD_ERR_INVALID_ARG;
   }
@@ -869,10 +887,11 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       if (e != cudaSuccess) return e;
     }
     if (phases) cudaEventRecord(T(l, PH_GATHER0), X);
-    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X);
+    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X,
+                      touch[l]);
     if (e != cudaSuccess) return e;
     if (phases) cudaEventRecord(T(l, PH_GATHER1), X);
-    launches += kGatherLaunches;
+    launches += kGatherLaunches - (touch[l] ? 0 : 1);
     return cudaEventRecord(c->ev_ready[s], X);
   };
   // Step 4 of layer l from scratch slot l % 2 (on the compute stream).

@@ -47,9 +47,13 @@ cudaError_t launch_score_bf16_query(const Dims& d, const void* q_bf16, const voi
 cudaError_t launch_score_select(const Dims& d, const void* q_spec, const void* k_dev,
                                 float* logits, float2* part, int32_t* counters, int32_t* idx,
                                 float* sel, float* lse, cudaStream_t st);
+// touch: first read one word per huge page of the host stores (worth it only
+// for stores backed by huge pages, i.e. from dd_host_alloc).
 cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
                           const int32_t* idx, void* k_buf, void* v_buf, int mode,
-                          cudaStream_t st);
+                          cudaStream_t st, bool touch);
+// True if p lies in a host store allocated by dd_host_alloc.
+bool in_huge_page_store(const void* p);
 // Where the attention reads the window's keys: row off + i (i < W) of each
 // unit's `stride` rows starting at p.
 struct WindowK {
@@ -94,6 +98,7 @@ struct LandmarkDims {
 dd_status resolve_landmarks(const dd_shape* s, int chunk, LandmarkDims* out);
 
 // Number of kernels each launcher enqueues.
+// (The gather is 2 launches with the huge-page touch, 1 without.)
 constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 2, kAttnLaunches = 2,
               kFixupLaunches = 1, kScoreSelectLaunches = 1;
 

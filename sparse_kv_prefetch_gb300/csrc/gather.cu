@@ -234,9 +234,9 @@ cudaError_t launch_lsu(const Dims& d, const void* kh, const void* vh, const int3
 
 cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
                           const int32_t* idx, void* k_buf, void* v_buf, int mode,
-                          cudaStream_t st) {
+                          cudaStream_t st, bool touch) {
   const int rb = d.d * d.elt;
-  if (mode == 0 || mode == 1) {
+  if (touch && (mode == 0 || mode == 1)) {
     static unsigned int* sinks[64] = {};  // device address of g_touch_sink, per device
     int dev = 0;
     cudaError_t e0 = cudaGetDevice(&dev);

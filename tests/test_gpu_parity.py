@@ -84,6 +84,16 @@ def test_host_store_from_dd_host_alloc():
     out = o.out.cpu().numpy()
     for u in range(w.units):
         check_unit_attention(w, s, u, idx[u], out)
+    # In the layer loop the gather over a huge-page store first reads one word per
+    # huge page (one more launch per layer); the output is the same.
+    ctx = dd.Ctx(dd_shape(w))
+    step_out = [torch.empty_like(o.out) for _ in range(2)]
+    ctx.decode_step(_layers(w, [s], step_out, 2), timing=True)
+    t = ctx.timings()
+    torch.cuda.synchronize()
+    assert t["launches"] == 2 * 6
+    assert torch.equal(step_out[0], o.out) and torch.equal(step_out[1], o.out)
+    ctx.close()
     dd.check_device()
 
 
@@ -205,8 +215,9 @@ def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
         assert torch.equal(outs_e[l], outs_b[l]), f"layer {l}: fused top-k != two kernels"
         assert torch.equal(outs_f[l], outs_b[l]), f"layer {l}: fused serial != two kernels"
         assert torch.equal(outs_a[l], ref[l % D]), f"layer {l}: step != per-layer calls"
-    assert t["n_layers"] == L and t["launches"] == L * 6 and t["topk_ms"] > 0
-    assert t_fused["launches"] == L * 5
+    # score, top-k, gather (the host-page touch only for huge-page stores), attention (2)
+    assert t["n_layers"] == L and t["launches"] == L * 5 and t["topk_ms"] > 0
+    assert t_fused["launches"] == L * 4
     assert t["step_ms"] > 0 and t["score_ms"] > 0 and t["gather_ms"] > 0
     dd.check_device()
     ctx.close()
@@ -304,7 +315,7 @@ def test_timing_ring_keeps_back_to_back_steps():
     torch.cuda.synchronize()
     ts = [ctx.timings(back=i) for i in range(3)]
     for t in ts:
-        assert t["n_layers"] == L and t["launches"] == 6 * L and t["step_ms"] > 0
+        assert t["n_layers"] == L and t["launches"] == 5 * L and t["step_ms"] > 0
         assert 0 < t["score_ms"] <= t["step_ms"]
     assert all(x > 0 for i in range(3) for x in ctx.score_times(L, back=i))
     with pytest.raises(dd.DDError):
@@ -322,7 +333,7 @@ def test_timing_ring_keeps_back_to_back_steps():
     torch.cuda.synchronize()
     assert t["step_ms"] > 0 and 0 < t["score_ms"] <= t["step_ms"]
     assert t["gather_ms"] == 0 and t["attn_ms"] == 0 and t["topk_ms"] == 0
-    assert t["launches"] == 6 * L
+    assert t["launches"] == 5 * L
     assert all(torch.equal(a, b) for a, b in zip(outs, ref))
     ctx.close()
 
