@@ -8,11 +8,17 @@ gather from pinned host memory and attention for every layer, on two streams.
 Prints one JSON line: layer-steps/s (device time, inputs resident), the same
 through the public API with host copies (e2e), the scoring kernel's HBM
 roofline, the gather's host-link bandwidth against a pinned-copy probe taken in
-the same process, the hidden fraction of the gather, and the fp64 oracle timed
-on the host cores as the CPU baseline.
+the same process, the hidden fraction of the gather, the recall of the
+prefetched rows, the step rate without per-layer events and as CUDA-graph
+replays, and the fp64 oracle timed on the host cores as the CPU baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--profile-case]
+                  [--workload NAME] [--schedule auto|overlap|late|pipeline|serial]
+                  [--landmarks C] [--fused-topk] [--correct-misses]
+                  [--gather-mode 0|1] [--host-alloc pinned|huge] [--profile-case]
+
+The schedule defaults to auto: overlap or serial, whichever a short calibration
+after the warm-up measures faster on this host.
 """
 from __future__ import annotations
 

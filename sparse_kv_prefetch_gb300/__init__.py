@@ -388,7 +388,8 @@ class Ctx:
 
     def capture_step(self, layers, compute, copy=None, **schedule):
         """Capture one decode step into a CUDA graph held by the context (the
-        step runs once directly first); replay it with replay_step."""
+        step runs once directly first); replay it with replay_step.  `compute`
+        must be a created stream (capture is not possible on the default one)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         _check(_lib().dd_ctx_capture_step(self._h, arr, len(arr), _stream(compute),
                                           None if copy is None else _stream(copy),
