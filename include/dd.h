@@ -51,6 +51,10 @@
  *    without synchronising.  Argument errors are reported synchronously
  *    (nothing is enqueued); a launch failure returns DD_ERR_CUDA; faults
  *    during execution surface at the caller's next synchronisation.
+ *  - Threads: the per-layer calls may be made from any thread; a dd_ctx is
+ *    used by one thread at a time (its steps share its scratch slots, events
+ *    and workspace, so steps of one context must also not run concurrently
+ *    on unrelated streams).
  *  - No exceptions cross this boundary.  The library has no CPU fallback.
  */
 #ifndef DD_H
