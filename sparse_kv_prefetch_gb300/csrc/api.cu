@@ -114,6 +114,8 @@ WsLayout ws_layout(const Dims& d) {
   off += align256((size_t)d.U * d.k * sizeof(float));
   w.counters = off;
   off += align256((size_t)d.U * sizeof(int32_t));
+  w.attn_counters = off;
+  off += align256((size_t)d.U * sizeof(int32_t));
   w.total = off;
   return w;
 }
@@ -693,9 +695,13 @@ dd_status dd_ctx_create(const dd_shape* shape, dd_ctx** out) {
   }
   ok = ok && cudaMalloc((void**)&c->lse, (size_t)d.B * d.Hq * sizeof(float)) == cudaSuccess;
   ok = ok && cudaMalloc(&c->ws, c->ws_lay.total) == cudaSuccess;
-  // The fused selection's counters start at zero (each launch leaves them so).
-  ok = ok && cudaMemset(static_cast<char*>(c->ws) + c->ws_lay.counters, 0,
-                        (size_t)d.U * sizeof(int32_t)) == cudaSuccess &&
+  // The fused selection's and the attention merge's counters start at zero
+  // (each launch leaves them so).
+  ok = ok &&
+       cudaMemset(static_cast<char*>(c->ws) + c->ws_lay.counters, 0,
+                  (size_t)d.U * sizeof(int32_t)) == cudaSuccess &&
+       cudaMemset(static_cast<char*>(c->ws) + c->ws_lay.attn_counters, 0,
+                  (size_t)d.U * sizeof(int32_t)) == cudaSuccess &&
        cudaDeviceSynchronize() == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
@@ -930,10 +936,10 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     const WindowK kw = layers[l].k_win ? window_buffer(layers[l].k_win, d)
                                        : window_in_cache(layers[l].k_dev, d);
     e = launch_attn(d, layers[l].q, kb, vb, kw, layers[l].v_win, layers[l].out, attn_o, attn_ml,
-                    A);
+                    A, reinterpret_cast<int32_t*>(ws + c->ws_lay.attn_counters));
     if (e != cudaSuccess) return e;
     if (phases) cudaEventRecord(T(l, PH_ATTN1), A);
-    launches += kAttnLaunches;
+    launches += kAttnLaunches - 1;  // the merge runs inside the partial kernel
     return cudaEventRecord(c->ev_free[s], A);
   };
 

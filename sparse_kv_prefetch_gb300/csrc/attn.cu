@@ -31,13 +31,37 @@ struct AttnGeom {
   static_assert(RS % kGroups == 0, "split must be a multiple of the row groups");
 };
 
-template <typename T, int D, int G>
+// The log-sum-exp merge of one output element over the nsplit partials of
+// its (request, query head) row; `CG` reads partials written by other CTAs of
+// the same launch past L1.
+template <bool CG>
+__device__ __forceinline__ float merge_splits(const float* part_o, const float2* part_ml,
+                                              size_t row, int nsplit, int D, int t) {
+  const float2* ml = part_ml + row * nsplit;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, (CG ? __ldcg(ml + s) : ml[s]).x);
+  float L = 0.f, acc = 0.f;
+  for (int s = 0; s < nsplit; ++s) {
+    const float2 v = CG ? __ldcg(ml + s) : ml[s];
+    const float w = __expf(v.x - M);
+    L = fmaf(w, v.y, L);
+    const float* po = part_o + (row * nsplit + s) * D + t;
+    acc = fmaf(w, CG ? __ldcg(po) : *po, acc);
+  }
+  return acc / L;
+}
+
+// MERGE: the last split CTA of each unit to finish (per-unit counters, zero
+// before the launch and after it) also merges the unit's G output rows, so no
+// separate merge launch is needed.
+template <typename T, int D, int G, bool MERGE>
 __global__ void __launch_bounds__(kAttnThreads)
     attn_partial_kernel(const uint4* __restrict__ q, const uint4* __restrict__ k_buf,
                         const uint4* __restrict__ v_buf, const uint4* __restrict__ k_win,
                         const uint4* __restrict__ v_win, float* __restrict__ part_o,
                         float2* __restrict__ part_ml, int kw_stride, int kw_off, int k, int W,
-                        int Hq, int Hkv, int nsplit, float scale) {
+                        int Hq, int Hkv, int nsplit, float scale, int32_t* __restrict__ counters,
+                        float* __restrict__ out) {
   using Geo = AttnGeom<T, D>;
   constexpr int VEC = Geo::kVec, LPR = Geo::kLpr, RPW = Geo::kRpw, NG = Geo::kGroups;
   constexpr int IT = Geo::kIt, V16 = LPR;
@@ -163,6 +187,21 @@ __global__ void __launch_bounds__(kAttnThreads)
     part_o[((size_t)(u * G + g) * nsplit + s) * D + t] = sum;
   }
   if (threadIdx.x < G) part_ml[(size_t)(u * G + threadIdx.x) * nsplit + s] = ml_sh[threadIdx.x];
+  if (!MERGE) return;
+
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(counters + u, 1) == nsplit - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  if (threadIdx.x == 0) counters[u] = 0;  // ready for the next launch
+  for (int x = threadIdx.x; x < G * D; x += kAttnThreads) {
+    const int g = x / D, t = x - g * D;
+    const size_t row = (size_t)u * G + g;  // = b H_q + h_kv G + g
+    out[row * D + t] = merge_splits<true>(part_o, part_ml, row, nsplit, D, t);
+  }
 }
 
 // One CTA of D threads per (request, query head): log-sum-exp merge of the splits.
@@ -170,32 +209,33 @@ __global__ void attn_merge_kernel(const float* __restrict__ part_o,
                                   const float2* __restrict__ part_ml, float* __restrict__ out,
                                   int nsplit, int D) {
   const int row = blockIdx.x, t = threadIdx.x;
-  const float2* ml = part_ml + (size_t)row * nsplit;
-  float M = -INFINITY;
-  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
-  float L = 0.f, acc = 0.f;
-  for (int s = 0; s < nsplit; ++s) {
-    const float w = __expf(ml[s].x - M);
-    L = fmaf(w, ml[s].y, L);
-    acc = fmaf(w, part_o[((size_t)row * nsplit + s) * D + t], acc);
-  }
-  out[(size_t)row * D + t] = acc / L;
+  out[(size_t)row * D + t] = merge_splits<false>(part_o, part_ml, row, nsplit, D, t);
 }
 
 template <typename T, int D, int G>
 cudaError_t launch_typed(const Dims& d, const void* q, const void* kb, const void* vb,
                          const WindowK& kw, const void* vw, float* out, float* po, float2* pml,
-                         cudaStream_t st) {
-  static unsigned long long prepared = 0, prepared_merge = 0;
-  cudaError_t e0 = prepare_kernel(attn_partial_kernel<T, D, G>, &prepared, 0);
-  if (e0 == cudaSuccess) e0 = prepare_kernel(attn_merge_kernel, &prepared_merge, 0);
-  if (e0 != cudaSuccess) return e0;
+                         int32_t* counters, cudaStream_t st) {
+  static unsigned long long prepared = 0, prepared_fused = 0, prepared_merge = 0;
   const float scale = 1.0f / sqrtf((float)d.d);
   const dim3 grid((unsigned)d.U, (unsigned)d.nsplit);
-  attn_partial_kernel<T, D, G><<<grid, kAttnThreads, 0, st>>>(
+  if (counters) {  // partials and merge in one launch
+    cudaError_t e0 = prepare_kernel(attn_partial_kernel<T, D, G, true>, &prepared_fused, 0);
+    if (e0 != cudaSuccess) return e0;
+    attn_partial_kernel<T, D, G, true><<<grid, kAttnThreads, 0, st>>>(
+        static_cast<const uint4*>(q), static_cast<const uint4*>(kb),
+        static_cast<const uint4*>(vb), static_cast<const uint4*>(kw.p),
+        static_cast<const uint4*>(vw), po, pml, kw.stride, kw.off, d.k, d.W, d.Hq, d.Hkv,
+        d.nsplit, scale, counters, out);
+    return cudaGetLastError();
+  }
+  cudaError_t e0 = prepare_kernel(attn_partial_kernel<T, D, G, false>, &prepared, 0);
+  if (e0 == cudaSuccess) e0 = prepare_kernel(attn_merge_kernel, &prepared_merge, 0);
+  if (e0 != cudaSuccess) return e0;
+  attn_partial_kernel<T, D, G, false><<<grid, kAttnThreads, 0, st>>>(
       static_cast<const uint4*>(q), static_cast<const uint4*>(kb), static_cast<const uint4*>(vb),
       static_cast<const uint4*>(kw.p), static_cast<const uint4*>(vw), po, pml, kw.stride, kw.off,
-      d.k, d.W, d.Hq, d.Hkv, d.nsplit, scale);
+      d.k, d.W, d.Hq, d.Hkv, d.nsplit, scale, nullptr, nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   attn_merge_kernel<<<(unsigned)(d.B * d.Hq), D, 0, st>>>(po, pml, out, d.nsplit, D);
@@ -205,12 +245,12 @@ cudaError_t launch_typed(const Dims& d, const void* q, const void* kb, const voi
 template <typename T, int D>
 cudaError_t launch_g(const Dims& d, const void* q, const void* kb, const void* vb,
                      const WindowK& kd, const void* vw, float* out, float* po, float2* pml,
-                     cudaStream_t st) {
+                     int32_t* cnt, cudaStream_t st) {
   switch (d.G) {
-    case 1: return launch_typed<T, D, 1>(d, q, kb, vb, kd, vw, out, po, pml, st);
-    case 2: return launch_typed<T, D, 2>(d, q, kb, vb, kd, vw, out, po, pml, st);
-    case 4: return launch_typed<T, D, 4>(d, q, kb, vb, kd, vw, out, po, pml, st);
-    case 8: return launch_typed<T, D, 8>(d, q, kb, vb, kd, vw, out, po, pml, st);
+    case 1: return launch_typed<T, D, 1>(d, q, kb, vb, kd, vw, out, po, pml, cnt, st);
+    case 2: return launch_typed<T, D, 2>(d, q, kb, vb, kd, vw, out, po, pml, cnt, st);
+    case 4: return launch_typed<T, D, 4>(d, q, kb, vb, kd, vw, out, po, pml, cnt, st);
+    case 8: return launch_typed<T, D, 8>(d, q, kb, vb, kd, vw, out, po, pml, cnt, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -219,14 +259,14 @@ cudaError_t launch_g(const Dims& d, const void* q, const void* kb, const void* v
 
 cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const void* v_buf,
                         const WindowK& k_dev, const void* v_win, float* out, float* part_o,
-                        float2* part_ml, cudaStream_t st) {
+                        float2* part_ml, cudaStream_t st, int32_t* counters) {
   if (d.dtype == DD_BF16) {
-    if (d.d == 64) return launch_g<bf16_t, 64>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, st);
-    if (d.d == 128) return launch_g<bf16_t, 128>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, st);
-    if (d.d == 256) return launch_g<bf16_t, 256>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, st);
+    if (d.d == 64) return launch_g<bf16_t, 64>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, counters, st);
+    if (d.d == 128) return launch_g<bf16_t, 128>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, counters, st);
+    if (d.d == 256) return launch_g<bf16_t, 256>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, counters, st);
   } else {
-    if (d.d == 64) return launch_g<float, 64>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, st);
-    if (d.d == 128) return launch_g<float, 128>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, st);
+    if (d.d == 64) return launch_g<float, 64>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, counters, st);
+    if (d.d == 128) return launch_g<float, 128>(d, q, k_buf, v_buf, k_dev, v_win, out, part_o, part_ml, counters, st);
   }
   return cudaErrorInvalidValue;
 }

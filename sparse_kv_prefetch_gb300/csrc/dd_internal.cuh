@@ -23,7 +23,7 @@ struct Dims {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t logits, part, attn_o, attn_ml, sel_true, counters, total;
+  size_t logits, part, attn_o, attn_ml, sel_true, counters, attn_counters, total;
 };
 
 dd_status resolve(const dd_shape* s, Dims* out);
@@ -66,9 +66,12 @@ inline WindowK window_in_cache(const void* k_dev, const Dims& d) {
 }
 inline WindowK window_buffer(const void* k_win, const Dims& d) { return WindowK{k_win, d.W, 0}; }
 
+// With counters ([U], zero before the launch and after it) the merge of the
+// splits runs inside the partial kernel (one launch); without, as a second
+// kernel.
 cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const void* v_buf,
                         const WindowK& k_win, const void* v_win, float* out, float* part_o,
-                        float2* part_ml, cudaStream_t st);
+                        float2* part_ml, cudaStream_t st, int32_t* counters = nullptr);
 
 // Miss correction (correct.cu): copy each row of the real query's top-k from
 // the prefetched buffer, or from the host store where the prediction missed.
@@ -99,6 +102,7 @@ dd_status resolve_landmarks(const dd_shape* s, int chunk, LandmarkDims* out);
 
 // Number of kernels each launcher enqueues.
 // (The gather is 2 launches with the huge-page touch, 1 without.)
+// (Attention is 1 launch in the layer loop, whose workspace keeps merge counters.)
 constexpr int kScoreLaunches = 1, kTopkLaunches = 1, kGatherLaunches = 2, kAttnLaunches = 2,
               kFixupLaunches = 1, kScoreSelectLaunches = 1;
 

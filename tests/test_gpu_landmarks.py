@@ -218,8 +218,8 @@ def test_landmark_decode_step_equals_calls_in_every_schedule(name):
         for l in range(L):
             assert torch.equal(outs[l], ref[l % D]), f"{sched}, layer {l}: != standalone calls"
     # score (reads a bf16 query itself), top-k (writes the chunks' rows), gather (pinned
-    # store: no host-page touch), attention (2)
-    per_layer = 1 + 1 + 1 + 2
+    # store: no host-page touch), attention (splits merged in the same kernel)
+    per_layer = 1 + 1 + 1 + 1
     assert t["n_layers"] == L and t["launches"] == L * per_layer
     with pytest.raises(dd.DDError):  # not combinable with miss correction
         ctx.decode_step(_layers(w, slots, runs["serial"], lms, L), compute=compute,
