@@ -12,7 +12,7 @@ import torch
 import sparse_kv_prefetch_gb300 as dd
 import synth
 from gpu_util import (Outputs, Slot, check_gather, check_unit_attention, check_unit_topk,
-                      dd_shape, oracle_selection_score, run_layer)
+                      dd_shape, oracle_selection_score, run_layer, sample_units)
 
 pytestmark = pytest.mark.gpu
 
@@ -110,12 +110,13 @@ def test_decode_step_with_correction(name):
     ctx = dd.Ctx(dd_shape(w))
     compute, copy = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
     compute.wait_stream(torch.cuda.current_stream())
-    for copy_stream in (copy, None):
+    for copy_stream, fused in ((copy, False), (None, False), (copy, True)):
         outs = [torch.full_like(ref_out[0], float("nan")) for _ in range(L)]
         layers = [dd.LayerIO(slots[l % D].q_spec, slots[l % D].q, slots[l % D].K,
                              slots[l % D].K_h, slots[l % D].V_h, slots[l % D].v_win, outs[l])
                   for l in range(L)]
-        ctx.decode_step(layers, compute=compute, copy=copy_stream, correct_misses=True)
+        ctx.decode_step(layers, compute=compute, copy=copy_stream, correct_misses=True,
+                        fused_topk=fused)
         misses, mass = ctx.correction_stats(L)
         torch.cuda.synchronize()
         for l in range(L):
@@ -123,3 +124,22 @@ def test_decode_step_with_correction(name):
             assert np.array_equal(misses[l], ref_miss[l % D]), f"layer {l}"
     dd.check_device()
     ctx.close()
+
+
+def test_full_size_correction_sampled_units():
+    """The 7B-32K layer at full size: the real query's top-k on sampled units
+    against the oracle, miss counts against the two index sets, corrected rows
+    bit-exact on those units."""
+    w = synth.C2
+    s, o = Slot(w), Outputs(w)
+    idx_true, kb, vb, miss, mass = _corrected(w, s, o)
+    spec, true = o.idx.cpu().numpy(), idx_true.cpu().numpy()
+    miss = miss.cpu().numpy()
+    units = sample_units(w.units, n=4, seed=11)
+    for u in units:
+        check_unit_topk(w, s, u, true[u], None, None, query=s.q_h)
+        assert miss[u] == w.top_k - np.isin(true[u], spec[u]).sum()
+    check_gather(w, s, true, kb, vb, units)
+    assert np.all(np.diff(true, axis=1) > 0)
+    del s, o, kb, vb
+    torch.cuda.empty_cache()

@@ -213,6 +213,18 @@ def test_landmark_decode_step_equals_calls_in_every_schedule(name):
         runs[sched] = outs
     with pytest.raises(dd.DDError):  # no key cache and no landmark selection
         ctx.decode_step(_layers(w, slots, outs, lms, L, k_wins), compute=compute)
+    # captured as a CUDA graph and replayed
+    outs = [torch.full((w.batch, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
+            for _ in range(L)]
+    ctx.capture_step(dd.Ctx.pack(_layers(w, slots, outs, lms, L, k_wins)), compute, copy=copy,
+                     landmarks=True)
+    for o in outs:
+        o.fill_(float("nan"))
+    compute.synchronize()
+    ctx.replay_step(compute)
+    ctx.replay_step(compute)
+    compute.synchronize()
+    runs["graph_no_k"] = outs
     torch.cuda.synchronize()
     for sched, outs in runs.items():
         for l in range(L):
