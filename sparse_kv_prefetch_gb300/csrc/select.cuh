@@ -11,6 +11,10 @@
 // Exact radix select on order-preserving 32-bit keys.  Each warp owns a
 // contiguous segment of the positions, so position order is the order
 // (warp, position within the warp's segment):
+//   sample  (n - W >= 16384) a histogram of one 128-position block in 16 sets
+//           a bucket b_low expected to keep ~1.5 k keys; one full pass B with
+//           b_low, and if it kept >= k keys without overflowing a list, b1 is
+//           found on the lists and pass A is skipped; else the exact passes:
 //   pass A  histogram of key bits 31..21 over the unit; the bucket b1 that
 //           holds the k-th largest key is found by a block scan from the top;
 //   pass B  every warp compacts the keys of its segment with top bits >= b1,
@@ -38,6 +42,8 @@ namespace sel {
 constexpr int kPer = 4;                // consecutive positions per lane per load
 constexpr int kWarpStep = 32 * kPer;  // positions per warp per load
 constexpr int kUnroll = 4;            // loads in flight per lane in passes A and B
+constexpr int kSampleEvery = 16;      // the sample: one warp step in 16
+constexpr int kSampleMin = 16384;     // positions below which no sample is taken
 
 template <int WARPS, int WCAP>
 struct Smem {
@@ -48,6 +54,7 @@ struct Smem {
   uint32_t wgt[WARPS];   // per warp: entries > T, then their exclusive prefix
   uint32_t weq[WARPS];   // per warp: entries == T, then their exclusive prefix
   uint32_t overflow;
+  uint32_t nsample;  // positions in the sample (sampled threshold)
   float lse[8];
   uint32_t keys[WCAP * WARPS];
   int32_t idxs[WCAP * WARPS];
@@ -372,35 +379,35 @@ __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int
   const int per_warp = ((span + WARPS - 1) / WARPS + kWarpStep - 1) / kWarpStep * kWarpStep;
   const int seg0 = min(span, warp * per_warp), seg1 = min(span, seg0 + per_warp);
 
-  // Pass A: bucket of the k-th largest key by its top 11 bits.  Each lane
+  // Pass A: histogram of the top 11 key bits over the whole unit.  Each lane
   // issues kUnroll loads before using any (memory-level parallelism).
-  for (int base = seg0; base < seg1; base += kWarpStep * kUnroll) {
-    uint32_t key[kUnroll][kPer];
+  auto pass_a = [&]() {
+    for (int base = seg0; base < seg1; base += kWarpStep * kUnroll) {
+      uint32_t key[kUnroll][kPer];
 #pragma unroll
-    for (int v = 0; v < kUnroll; ++v) {
-      const int j0 = base + v * kWarpStep + lane * kPer;
-      if (j0 < seg1) src.load4(j0, key[v]);
+      for (int v = 0; v < kUnroll; ++v) {
+        const int j0 = base + v * kWarpStep + lane * kPer;
+        if (j0 < seg1) src.load4(j0, key[v]);
+      }
+#pragma unroll
+      for (int v = 0; v < kUnroll; ++v) {
+        const int j0 = base + v * kWarpStep + lane * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+          if (j0 + e < seg1) atomicAdd(&sm.hist[key[v][e] >> 21], 1u);
+      }
     }
-#pragma unroll
-    for (int v = 0; v < kUnroll; ++v) {
-      const int j0 = base + v * kWarpStep + lane * kPer;
-#pragma unroll
-      for (int e = 0; e < kPer; ++e)
-        if (j0 + e < seg1) atomicAdd(&sm.hist[key[v][e] >> 21], 1u);
-    }
-  }
-  sync<WARPS>();
-  find_bin<WARPS>(sm.hist, 2048, (uint32_t)k, sm.wt, sm.res);
-  const uint32_t b1 = sm.res[0];
-  uint32_t k_rem = (uint32_t)k - sm.res[1];
-  sync<WARPS>();
+    sync<WARPS>();
+  };
 
-  // Pass B: each warp compacts its keys in buckets >= b1, in position order.
-  {
+  // Pass B: each warp compacts its keys whose top bits are >= thr, in
+  // position order, into its own shared-memory list.
+  auto pass_b = [&](uint32_t thr) {
     uint32_t* keys = sm.keys + warp * WCAP;
     int32_t* idxs = sm.idxs + warp * WCAP;
     uint32_t n_w = 0;
     bool over = false;
+    const unsigned lt_mask = (1u << lane) - 1u;
     for (int base = seg0; base < seg1 && !over; base += kWarpStep * kUnroll) {
       uint32_t key[kUnroll][kPer];
 #pragma unroll
@@ -410,7 +417,6 @@ __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int
       }
       // The kUnroll groups in position order: group v covers
       // [base + v kWarpStep, base + (v + 1) kWarpStep).
-      const unsigned lt_mask = (1u << lane) - 1u;
 #pragma unroll
       for (int v = 0; v < kUnroll; ++v) {
         const int j0 = base + v * kWarpStep + lane * kPer;
@@ -419,7 +425,7 @@ __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int
         unsigned any = 0;
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {
-          f[e] = (j0 + e < seg1) && (key[v][e] >> 21) >= b1;
+          f[e] = (j0 + e < seg1) && (key[v][e] >> 21) >= thr;
           bal[e] = __ballot_sync(0xffffffffu, f[e]);
           any |= bal[e];
         }
@@ -451,8 +457,81 @@ __device__ void select_unit(Smem<WARPS, WCAP>& sm, const float* lg, int ldn, int
       sm.wcnt[warp] = n_w;
       if (over) atomicOr(&sm.overflow, 1u);
     }
+    sync<WARPS>();
+  };
+
+  uint32_t b1 = 0, k_rem = 0;
+  bool ready = false;  // lists hold every key of bucket >= b1; b1, k_rem exact
+  if (span >= kSampleMin) {
+    // Sampled threshold: a histogram of one warp step in kSampleEvery gives a
+    // bucket b_low that keeps about 1.5 times the expected number of top-k
+    // keys above it; one full pass compacts every key of bucket >= b_low.  If
+    // that holds at least k keys (so all of the top k) and no list overflowed,
+    // the exact bucket b1 comes from the lists alone: one pass over the
+    // logits instead of two.  Otherwise the exact two passes run.
+    if (threadIdx.x == 0) sm.nsample = 0;
+    sync<WARPS>();
+    uint32_t mine = 0;
+    for (int base = seg0; base < seg1; base += kWarpStep * kSampleEvery * kUnroll) {
+      uint32_t key[kUnroll][kPer];
+#pragma unroll
+      for (int v = 0; v < kUnroll; ++v) {
+        const int j0 = base + v * kWarpStep * kSampleEvery + lane * kPer;
+        if (j0 < seg1) src.load4(j0, key[v]);
+      }
+#pragma unroll
+      for (int v = 0; v < kUnroll; ++v) {
+        const int j0 = base + v * kWarpStep * kSampleEvery + lane * kPer;
+#pragma unroll
+        for (int e = 0; e < kPer; ++e)
+          if (j0 + e < seg1) {
+            atomicAdd(&sm.hist[key[v][e] >> 21], 1u);
+            ++mine;
+          }
+      }
+    }
+    if (mine) atomicAdd(&sm.nsample, mine);
+    sync<WARPS>();
+    const uint32_t ns = sm.nsample;
+    const uint32_t ks = (uint32_t)(((unsigned long long)k * ns * 3) / (2ull * span)) + 8;
+    if (ks <= ns) {
+      find_bin<WARPS>(sm.hist, 2048, ks, sm.wt, sm.res);
+      const uint32_t b_low = sm.res[0];
+      sync<WARPS>();
+      pass_b(b_low);
+      uint32_t cand = 0;
+      for (int w = 0; w < WARPS; ++w) cand += sm.wcnt[w];
+      if (!sm.overflow && cand >= (uint32_t)k) {
+        // Exact b1 and the count above it, from the candidates.
+        for (int i = threadIdx.x; i < 2048; i += WARPS * 32) sm.hist[i] = 0;
+        sync<WARPS>();
+        {
+          const uint32_t* keys = sm.keys + warp * WCAP;
+          const int cnt = (int)sm.wcnt[warp];
+          for (int e = lane; e < cnt; e += 32) atomicAdd(&sm.hist[keys[e] >> 21], 1u);
+        }
+        sync<WARPS>();
+        find_bin<WARPS>(sm.hist, 2048, (uint32_t)k, sm.wt, sm.res);
+        b1 = sm.res[0];
+        k_rem = (uint32_t)k - sm.res[1];
+        ready = true;
+      }
+      sync<WARPS>();
+    }
+    if (!ready) {
+      if (threadIdx.x == 0) sm.overflow = 0;
+      for (int i = threadIdx.x; i < 2048; i += WARPS * 32) sm.hist[i] = 0;
+      sync<WARPS>();
+    }
   }
-  sync<WARPS>();
+  if (!ready) {
+    pass_a();
+    find_bin<WARPS>(sm.hist, 2048, (uint32_t)k, sm.wt, sm.res);
+    b1 = sm.res[0];
+    k_rem = (uint32_t)k - sm.res[1];
+    sync<WARPS>();
+    pass_b(b1);
+  }
 
   uint32_t T;
   if (!sm.overflow) {

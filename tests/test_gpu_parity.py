@@ -167,6 +167,32 @@ def test_exact_ties_take_lowest_positions(n):
     ctx.close()
 
 
+def test_sampled_threshold_falls_back_when_the_sample_misleads():
+    """The selection first estimates its threshold from one 128-position block
+    in 16 (for n - W = 32704 and 16 warps: the blocks p mod 2048 < 128).  Forty
+    strong keys placed exactly there make the sample's estimate keep fewer
+    than k candidates; the exact two-pass selection must then take over, and
+    the result must still be the exact top-k."""
+    w = C2.scaled(batch=1, n_q_heads=2, n_kv_heads=2, ctx_len=32768, top_k=128, window=64,
+                  n_planted=0, plant_mode=synth.PLANT_NONE)
+    s = Slot(w)
+    K = s.K_h.view(w.units, w.ctx_len, w.head_dim)
+    q = s.q_spec_h.view(w.units, w.head_dim).float()
+    pos = torch.tensor([(i % 16) * 2048 + (i * 37) % 128 for i in range(40)])
+    assert bool((pos % 2048 < 128).all()) and len(set(pos.tolist())) == 40
+    for u in range(w.units):
+        strong = (q[u] / q[u].norm() * 3 * w.head_dim ** 0.5).to(K.dtype)
+        K[u, pos] = strong
+    s.to_device()
+    o = Outputs(w)
+    run_layer(w, s, o)
+    torch.cuda.synchronize()
+    idx = o.idx.cpu().numpy()
+    for u in range(w.units):
+        assert set(pos.tolist()) <= set(idx[u].tolist())
+        check_unit_topk(w, s, u, idx[u], o.sel.cpu().numpy()[u], o.lse.cpu().numpy())
+
+
 def _layers(w, slots, outs, L):
     return [dd.LayerIO(slots[l % len(slots)].q_spec, slots[l % len(slots)].q,
                        slots[l % len(slots)].K, slots[l % len(slots)].K_h,
