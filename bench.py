@@ -45,7 +45,7 @@ FALLBACK_HBM_GBS = 6800.0
 # profiles/ (batch 2: 64 units), scaled by units to the 7B-32K layer (256
 # units); traffic grows with the units processed.  Keyed by (workload, top-k
 # fused into the scoring kernel); absent where no capture of that kernel exists.
-SCORE_TRAFFIC_BYTES = {("c2-7b-32k", False): 544.71e6 * 256 / 64}
+SCORE_TRAFFIC_BYTES = {("c2-7b-32k", False): 545.35e6 * 256 / 64}
 
 
 def parse():
