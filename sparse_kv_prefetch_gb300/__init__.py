@@ -9,6 +9,25 @@ Buffers are torch tensors (device tensors for device arguments, page-locked CPU
 tensors for the host KV store) or raw integer addresses.  Streams are
 ``torch.cuda.Stream`` objects, raw ``cudaStream_t`` integers, or None for the
 current torch stream.
+
+A decode step over L layers::
+
+    import torch, sparse_kv_prefetch_gb300 as dd
+    shape = dd.Shape(B, H_q, H_kv, d, n, k, W, dd.DD_BF16)
+    ctx = dd.Ctx(shape)                     # scratch slots, workspace, events
+    layers = [dd.LayerIO(q_spec[l], q[l],   # device [B][H_q][d]
+                         K_dev[l],          # device [B][H_kv][n][d]
+                         K_host[l], V_host[l],  # pinned host [B][H_kv][n][d]
+                         V_win[l],          # device [B][H_kv][W][d]
+                         out[l])            # device fp32 [B][H_q][d]
+              for l in range(L)]
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
+    ctx.decode_step(layers, compute=compute, copy=copy)   # asynchronous
+
+or, for fixed buffers, ``ctx.capture_step(layers, compute, copy=copy)`` once and
+``ctx.replay_step(compute)`` per step.  Landmark (chunk) selection:
+``build_landmarks`` per layer, ``ctx.set_landmark_chunk(c)``, the landmarks in
+``LayerIO(..., landmarks=L)`` and ``decode_step(..., landmarks=True)``.
 """
 from __future__ import annotations
 
