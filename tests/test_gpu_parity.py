@@ -384,6 +384,11 @@ def test_full_size_layer_sampled_units(name):
     ctx.decode_step(_layers(w, [s], outs, 2), compute=compute, copy=copy)
     torch.cuda.synchronize()
     assert torch.equal(outs[0], o.out) and torch.equal(outs[1], o.out)
+    # the fused form of steps 1-2 (its last-CTA selection samples at these sizes too)
+    fused = [torch.full_like(o.out, float("nan"))]
+    ctx.decode_step(_layers(w, [s], fused, 1), compute=compute, copy=copy, fused_topk=True)
+    torch.cuda.synchronize()
+    assert torch.equal(fused[0], o.out)
     idx, sel, lse = o.idx.cpu().numpy(), o.sel.cpu().numpy(), o.lse.cpu().numpy()
     out = o.out.cpu().numpy()
     units = sample_units(w.units, n=5, seed=w.cfg_id)
