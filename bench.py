@@ -17,8 +17,8 @@ replays, and the fp64 oracle timed on the host cores as the CPU baseline.
                   [--landmarks C] [--fused-topk] [--correct-misses]
                   [--gather-mode 0|1] [--host-alloc pinned|huge] [--profile-case]
 
-The schedule defaults to auto: overlap or serial, whichever a short calibration
-after the warm-up measures faster on this host.
+The schedule defaults to auto: overlap, serial or pipeline, whichever a short
+calibration after the warm-up measures fastest on this host and workload.
 """
 from __future__ import annotations
 
@@ -71,9 +71,10 @@ def parse():
                    help="overlap: gather l+1 beside attention l; late: gather l+1 after "
                         "attention l; pipeline: gather and attention of each layer on the "
                         "copy stream; serial: every phase in order on one stream; auto: "
-                        "overlap or serial, whichever a short calibration after the warm-up "
-                        "measures faster (scoring and the host gather slow each other when "
-                        "they run together, by an amount that varies between hosts)")
+                        "overlap, serial or pipeline, whichever a short calibration after the "
+                        "warm-up measures fastest (scoring and the host gather slow each other "
+                        "when they run together, by an amount that varies between hosts and "
+                        "workloads)")
     p.add_argument("--correct-misses", action="store_true",
                    help="correct prediction misses in every timed layer (DD_STEP_CORRECT_MISSES)")
     p.add_argument("--landmarks", type=int, default=0, metavar="C",
@@ -479,10 +480,12 @@ def run_ours(args, rank, world):
         step(sched_copy)
     torch.cuda.synchronize()
     if args.schedule == "auto":
-        # Calibration: overlap and serial alternately, 3 untimed-inside steps each, twice.
-        cal = {"overlap": 0.0, "serial": 0.0}
+        # Calibration: overlap, serial and pipeline in turn, 3 steps each, twice.
+        cands = (("overlap", copy, False), ("serial", None, False), ("pipeline", copy, True))
+        cal = {name: 0.0 for name, _, _ in cands}
         for _ in range(2):
-            for name, cs in (("overlap", copy), ("serial", None)):
+            for name, cs, pp in cands:
+                pipe = pp  # read by step()
                 c0 = torch.cuda.Event(enable_timing=True)
                 c1 = torch.cuda.Event(enable_timing=True)
                 c0.record(compute)
@@ -491,15 +494,16 @@ def run_ours(args, rank, world):
                 c1.record(compute)
                 torch.cuda.synchronize()
                 cal[name] += c0.elapsed_time(c1) / 6
+        names = [name for name, _, _ in cands]
         pick = min(cal, key=cal.get)
         if world > 1:  # every rank runs the same schedule: rank 0's choice
             import torch.distributed as dist
-            t = torch.tensor([0 if pick == "overlap" else 1], device=dev)
+            t = torch.tensor([names.index(pick)], device=dev)
             dist.broadcast(t, 0)
-            pick = "overlap" if int(t) == 0 else "serial"
-        sched_copy = copy if pick == "overlap" else None
-        args.schedule_chosen = (f"{pick} (auto; calibration ms per step: overlap "
-                                f"{cal['overlap']:.2f}, serial {cal['serial']:.2f})")
+            pick = names[int(t)]
+        _, sched_copy, pipe = cands[names.index(pick)]
+        args.schedule_chosen = (f"{pick} (auto; calibration ms per step: "
+                                + ", ".join(f"{k} {v:.2f}" for k, v in cal.items()) + ")")
     n_serial = max(3, args.steps // 4)
     n_phase = max(3, args.steps // 2)
     ctx.set_timing_depth(max(args.steps, n_serial, n_phase))
