@@ -13,12 +13,12 @@ prefetched rows, the step rate without per-layer events and as CUDA-graph
 replays, and the fp64 oracle timed on the host cores as the CPU baseline.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--schedule auto|overlap|late|pipeline|serial]
+                  [--workload NAME] [--schedule auto|overlap|late|pipeline|serial|guarded]
                   [--landmarks C] [--fused-topk] [--correct-misses]
                   [--gather-mode 0|1] [--host-alloc pinned|huge] [--profile-case]
 
-The schedule defaults to auto: overlap, serial or pipeline, whichever a short
-calibration after the warm-up measures fastest on this host and workload.
+The schedule defaults to auto: overlap, serial, pipeline or guarded, whichever a
+short calibration after the warm-up measures fastest on this host and workload.
 """
 from __future__ import annotations
 
@@ -67,11 +67,13 @@ def parse():
     p.add_argument("--slots", type=int, default=0,
                    help="override the number of distinct layer slots (memory-limited runs)")
     p.add_argument("--schedule", default="auto",
-                   choices=["auto", "overlap", "late", "pipeline", "serial"],
+                   choices=["auto", "overlap", "late", "pipeline", "serial", "guarded"],
                    help="overlap: gather l+1 beside attention l; late: gather l+1 after "
                         "attention l; pipeline: gather and attention of each layer on the "
-                        "copy stream; serial: every phase in order on one stream; auto: "
-                        "overlap, serial or pipeline, whichever a short calibration after the "
+                        "copy stream; serial: every phase in order on one stream; guarded: "
+                        "overlap, but each scoring waits for the previous layer's gather; "
+                        "auto: overlap, serial, pipeline or guarded, whichever a short "
+                        "calibration after the "
                         "warm-up measures fastest (scoring and the host gather slow each other "
                         "when they run together, by an amount that varies between hosts and "
                         "workloads)")
@@ -324,6 +326,7 @@ def run_ours(args, rank, world):
     ctx = dd.Ctx(shape)
     late = bool(args.late_gather) or args.schedule == "late"
     pipe = args.schedule == "pipeline"
+    guard = args.schedule == "guarded"
     if args.copy_priority == "high":
         compute, copy = torch.cuda.Stream(), torch.cuda.Stream(priority=-1)
     else:
@@ -465,7 +468,7 @@ def run_ours(args, rank, world):
         ctx.decode_step(layers, compute=compute, copy=copy_stream, timing=timing,
                         late_gather=late, pipeline=pipe, gather_mode=args.gather_mode,
                         correct_misses=args.correct_misses, landmarks=bool(C),
-                        fused_topk=args.fused_topk)
+                        fused_topk=args.fused_topk, guarded=guard)
 
     def recorded(n_steps):
         """Phase times and per-layer scoring times of the last n timed steps,
@@ -481,11 +484,12 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
     if args.schedule == "auto":
         # Calibration: overlap, serial and pipeline in turn, 3 steps each, twice.
-        cands = (("overlap", copy, False), ("serial", None, False), ("pipeline", copy, True))
-        cal = {name: 0.0 for name, _, _ in cands}
+        cands = (("overlap", copy, False, False), ("serial", None, False, False),
+                 ("pipeline", copy, True, False), ("guarded", copy, False, True))
+        cal = {name: 0.0 for name, _, _, _ in cands}
         for _ in range(2):
-            for name, cs, pp in cands:
-                pipe = pp  # read by step()
+            for name, cs, pp, gg in cands:
+                pipe, guard = pp, gg  # read by step()
                 c0 = torch.cuda.Event(enable_timing=True)
                 c1 = torch.cuda.Event(enable_timing=True)
                 c0.record(compute)
@@ -494,14 +498,14 @@ def run_ours(args, rank, world):
                 c1.record(compute)
                 torch.cuda.synchronize()
                 cal[name] += c0.elapsed_time(c1) / 6
-        names = [name for name, _, _ in cands]
+        names = [name for name, _, _, _ in cands]
         pick = min(cal, key=cal.get)
         if world > 1:  # every rank runs the same schedule: rank 0's choice
             import torch.distributed as dist
             t = torch.tensor([names.index(pick)], device=dev)
             dist.broadcast(t, 0)
             pick = names[int(t)]
-        _, sched_copy, pipe = cands[names.index(pick)]
+        _, sched_copy, pipe, guard = cands[names.index(pick)]
         args.schedule_chosen = (f"{pick} (auto; calibration ms per step: "
                                 + ", ".join(f"{k} {v:.2f}" for k, v in cal.items()) + ")")
     n_serial = max(3, args.steps // 4)
@@ -538,7 +542,7 @@ def run_ours(args, rank, world):
     # The same steps as one CUDA graph launch each (captured once).
     ctx.capture_step(layers, compute, copy=sched_copy, late_gather=late, pipeline=pipe,
                      gather_mode=args.gather_mode, correct_misses=args.correct_misses,
-                     landmarks=bool(C), fused_topk=args.fused_topk)
+                     landmarks=bool(C), fused_topk=args.fused_topk, guarded=guard)
     ctx.replay_step(compute)
     torch.cuda.synchronize()
     ev4, ev5 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -582,7 +586,7 @@ def run_ours(args, rank, world):
         ctx.decode_step(layers_e2e, compute=compute, copy=sched_copy, late_gather=late,
                         pipeline=pipe,
                         gather_mode=args.gather_mode, correct_misses=args.correct_misses,
-                        landmarks=bool(C), fused_topk=args.fused_topk)
+                        landmarks=bool(C), fused_topk=args.fused_topk, guarded=guard)
         with torch.cuda.stream(compute):
             out_h.copy_(outs, non_blocking=True)
     for _ in range(2):

@@ -367,6 +367,10 @@ enum {
                               (no separate top-k launch; same results).  Off by
                               default: on GB300 the two-kernel form measured
                               faster on the MHA and GQA workloads */
+  DD_STEP_GATHER_BESIDE_ATTN = 256,   /* overlapped schedule in which the scoring
+                                         of layer l+1 waits for the gather of layer
+                                         l: each gather overlaps only the previous
+                                         layer's attention, never a scoring kernel */
   DD_STEP_DEBUG_DELAY_COPY = 512,     /* test hook: a 50 us GPU sleep before each
                                          gather, on the stream that runs it */
   DD_STEP_DEBUG_DELAY_COMPUTE = 1024, /* test hook: the same before each attention;

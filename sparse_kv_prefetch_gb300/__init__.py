@@ -49,6 +49,7 @@ DD_STEP_CORRECT_MISSES = 16
 DD_STEP_LANDMARKS = 32
 DD_STEP_TIMING_LIGHT = 64
 DD_STEP_FUSED_TOPK = 128
+DD_STEP_GATHER_BESIDE_ATTN = 256
 DD_STEP_DEBUG_DELAY_COPY = 512
 DD_STEP_DEBUG_DELAY_COMPUTE = 1024
 
@@ -381,21 +382,23 @@ class Ctx:
     def decode_step(self, layers, compute=None, copy=None, timing=False,
                     late_gather: bool = False, gather_mode: int = 0, pipeline: bool = False,
                     correct_misses: bool = False, landmarks: bool = False,
-                    fused_topk: bool = False, debug_delay: str = ""):
+                    fused_topk: bool = False, debug_delay: str = "", guarded: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
         arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
         # timing: False, True (every phase) or "light" (step and scoring only)
         flags = self._flags(late_gather, gather_mode, pipeline, correct_misses, landmarks,
-                            fused_topk, timing, debug_delay)
+                            fused_topk, timing, debug_delay, guarded)
         _check(_lib().dd_decode_step(self._h, arr, len(arr), cs, xs, flags), "dd_decode_step")
         self._keep = arr
 
     @staticmethod
     def _flags(late_gather=False, gather_mode=0, pipeline=False, correct_misses=False,
-               landmarks=False, fused_topk=False, timing=False, debug_delay=""):
+               landmarks=False, fused_topk=False, timing=False, debug_delay="",
+               guarded=False):
         return ((DD_STEP_DEBUG_DELAY_COPY if "copy" in debug_delay else 0)
+                | (DD_STEP_GATHER_BESIDE_ATTN if guarded else 0)
                 | (DD_STEP_DEBUG_DELAY_COMPUTE if "compute" in debug_delay else 0)
                 | (DD_STEP_TIMING_LIGHT if timing == "light" else DD_STEP_TIMING if timing else 0)
                 | (DD_STEP_LATE_GATHER if late_gather else 0)

@@ -973,7 +973,13 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
     DD_TRY(score_topk(0));
     DD_TRY(gather(0));
     const bool late = (flags & DD_STEP_LATE_GATHER) != 0;
+    const bool guarded = (flags & DD_STEP_GATHER_BESIDE_ATTN) != 0;
     for (int l = 0; l < n_layers; ++l) {
+      // Guarded: the next scoring starts only once layer l's gather is done,
+      // so a gather runs beside the previous layer's attention, never beside
+      // a scoring kernel (the two slow each other down through the memory
+      // system's address translation).
+      if (guarded) DD_TRY(cudaStreamWaitEvent(C, c->ev_ready[l & 1], 0));
       if (l + 1 < n_layers) DD_TRY(score_topk(l + 1));
       if (l + 1 < n_layers && !late) DD_TRY(gather(l + 1));
       DD_TRY(attend(l));

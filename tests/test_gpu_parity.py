@@ -233,6 +233,9 @@ def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
     t_fused = ctx.timings()
     outs_f = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
     ctx.decode_step(_layers(w, slots, outs_f, L), compute=compute, copy=None, fused_topk=True)
+    # guarded: each scoring waits for the previous layer's gather
+    outs_g = [torch.full_like(outs_a[0], float("nan")) for _ in range(L)]
+    ctx.decode_step(_layers(w, slots, outs_g, L), compute=compute, copy=copy, guarded=True)
     torch.cuda.synchronize()
     for l in range(L):
         assert torch.equal(outs_a[l], outs_b[l]), f"layer {l}: overlapped != serial"
@@ -240,6 +243,7 @@ def test_decode_step_overlapped_equals_serial_and_per_layer_calls(name):
         assert torch.equal(outs_d[l], outs_b[l]), f"layer {l}: pipeline != serial"
         assert torch.equal(outs_e[l], outs_b[l]), f"layer {l}: fused top-k != two kernels"
         assert torch.equal(outs_f[l], outs_b[l]), f"layer {l}: fused serial != two kernels"
+        assert torch.equal(outs_g[l], outs_b[l]), f"layer {l}: guarded != serial"
         assert torch.equal(outs_a[l], ref[l % D]), f"layer {l}: step != per-layer calls"
     # score, top-k, gather (the host-page touch only for huge-page stores), attention (the
     # merge of its splits inside the same kernel)
@@ -307,7 +311,7 @@ def test_captured_step_replays_bit_identical(name):
     ref = [torch.empty((w.batch, w.n_q_heads, w.head_dim), device="cuda") for _ in range(L)]
     ctx.decode_step(_layers(w, slots, ref, L), compute=compute, copy=copy)
     for sched in (dict(copy=copy), dict(copy=None), dict(copy=copy, pipeline=True),
-                  dict(copy=copy, fused_topk=True)):
+                  dict(copy=copy, fused_topk=True), dict(copy=copy, guarded=True)):
         outs = [torch.full_like(ref[0], float("nan")) for _ in range(L)]
         layers = dd.Ctx.pack(_layers(w, slots, outs, L))
         ctx.capture_step(layers, compute, **sched)

@@ -38,7 +38,7 @@ def test_delayed_streams_keep_every_schedule_exact(w):
     ref = [torch.empty((w.batch, w.n_q_heads, w.head_dim), device="cuda") for _ in range(L)]
     ctx.decode_step(_layers(w, slots, ref, L), compute=compute, copy=None)
     for delay in ("copy", "compute", "copy+compute"):
-        for sched in (dict(), dict(late_gather=True), dict(pipeline=True)):
+        for sched in (dict(), dict(late_gather=True), dict(pipeline=True), dict(guarded=True)):
             outs = [torch.full_like(ref[0], float("nan")) for _ in range(L)]
             ctx.decode_step(_layers(w, slots, outs, L), compute=compute, copy=copy,
                             debug_delay=delay, **sched)
