@@ -300,3 +300,27 @@ def test_chunk_change_reuses_workspace_and_fused_selection_still_agrees():
             assert torch.equal(r[l], runs[0][l])
     dd.check_device()
     ctx.close()
+
+
+@pytest.mark.parametrize("dtype", [synth.F32, synth.BF16])
+def test_every_chunk_selected_gives_every_row(dtype):
+    """k = n - W: every chunk is selected, the rows are 0 .. n - W - 1 in
+    order, and the attention equals the oracle's over all n positions."""
+    base = C1 if dtype == synth.F32 else C2
+    w = base.scaled(batch=1, n_q_heads=4, n_kv_heads=2, head_dim=64, ctx_len=528, top_k=512,
+                    window=16)
+    chunk = 16
+    orc = oracle.get()
+    s = Slot(w)
+    lmk = Landmarks(w, s, chunk)
+    rows = lmk.idx.cpu().numpy()
+    for u in range(w.units):
+        assert rows[u].tolist() == list(range(w.ctx_len - w.window))
+    o = Outputs(w)
+    shp = dd_shape(w)
+    dd.gather_h2d(shp, s.K_h, s.V_h, lmk.idx, o.k_buf, o.v_buf)
+    dd.sparse_decode_attn(shp, s.q, o.k_buf, o.v_buf, s.K, s.v_win, o.out, o.ws)
+    torch.cuda.synchronize()
+    out = o.out.cpu().numpy()
+    for u in range(w.units):
+        check_unit_attention(w, s, u, rows[u], out, orc)
