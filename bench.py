@@ -1,21 +1,28 @@
 """Benchmark of the predictive sparse-KV decode step on one GB300.
 
-A step is one dd_decode_step over all L layers of the LLaMA-2-7B-shaped
-workload (32 layers cycling 8 distinct layer slots, batch 8, 32 MHA heads x
-128, context 32768, top-k 128 + a 64-token window, bf16): scoring, top-k,
-gather from pinned host memory and attention for every layer, on two streams.
+A step is one dd_decode_step over all L layers of a workload: scoring, top-k,
+gather from the pinned host KV store and attention for every layer, on two
+streams.  The default workload is the largest one that fits one GPU and its
+host as stated: the high-concurrency GQA shape (32 layers cycling 4 distinct
+layer slots, batch 32, 32 query / 8 KV heads x 128, context 131072, top-k
+2048 per KV head, no window, bf16; 32 GiB of keys in HBM, 64 GiB of host K/V).
+The 13B-shaped 64K workload would need 160 GiB of page-locked host memory for
+its 8 layer slots, more than a 199 GiB host can lock beside everything else.
 
-Prints one JSON line: layer-steps/s (device time, inputs resident), the same
+Prints one JSON line: layer-steps/s (device time, inputs resident; the median
+of several back-to-back regions of K steps, with their min and max), the same
 through the public API with host copies (e2e), the scoring kernel's HBM
 roofline, the gather's host-link bandwidth against a pinned-copy probe taken in
-the same process, the hidden fraction of the gather, the recall of the
-prefetched rows, the step rate without per-layer events and as CUDA-graph
-replays, and the fp64 oracle timed on the host cores as the CPU baseline.
+the same process, the hidden fraction of the gather (event-free overlapped and
+serial regions, interleaved), the recall of the prefetched rows, the step rate
+as CUDA-graph replays, and the fp64 oracle timed on the host cores as the CPU
+baseline.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--schedule auto|overlap|late|pipeline|serial|guarded]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--repeats R]
+                  [--impl ours|reference] [--workload NAME]
+                  [--schedule auto|overlap|late|pipeline|serial|guarded]
                   [--landmarks C] [--fused-topk] [--correct-misses]
-                  [--gather-mode 0|1] [--host-alloc pinned|huge] [--profile-case]
+                  [--gather-mode 0|1] [--host-alloc huge|pinned] [--profile-case]
 
 The schedule defaults to auto: overlap, serial, pipeline or guarded, whichever a
 short calibration after the warm-up measures fastest on this host and workload.
@@ -54,14 +61,17 @@ def parse():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    p.add_argument("--workload", default=synth.C2.name, choices=list(synth.WORKLOADS))
+    p.add_argument("--workload", default=synth.C5.name, choices=list(synth.WORKLOADS))
+    p.add_argument("--repeats", type=int, default=5,
+                   help="back-to-back timed regions of --steps steps; value is the median")
     p.add_argument("--profile-case", action="store_true",
                    help="small case for ncu captures: batch 2, 2 layers, 1 slot")
     p.add_argument("--gather-mode", type=int, default=None, choices=[0, 1],
                    help="0: bulk-copy gather, 1: load/store gather (default: 0, or 1 with "
                         "--landmarks, where whole chunks make it the faster one)")
-    p.add_argument("--host-alloc", default="pinned", choices=["huge", "pinned"],
-                   help="host KV store: dd_host_alloc huge pages, or torch pinned memory")
+    p.add_argument("--host-alloc", default="huge", choices=["huge", "pinned"],
+                   help="host KV store: dd_host_alloc (transparent huge pages, locked and "
+                        "registered) or torch pinned memory (64 KiB pages)")
     p.add_argument("--copy-priority", default="high", choices=["high", "low"],
                    help="priority of the copy stream relative to the compute stream")
     p.add_argument("--slots", type=int, default=0,
@@ -298,12 +308,12 @@ def run_ours(args, rank, world):
                               w.top_k, w.window)
     D, L = w.n_slots, w.n_layers
 
-    # Host store (pinned) and the device-resident key cache, per layer slot.
+    # Host store and the device-resident key cache, per layer slot.  The
+    # store defaults to dd_host_alloc's huge pages: with 64 KiB pages every
+    # long-context gather needs hundreds of thousands of page translations,
+    # which slows the gather and the scoring beside it.
     huge0 = anon_huge_bytes()
-    # Pinned memory from torch by default.  dd_host_alloc's huge-page store
-    # made the gather faster in most runs on GB300, but the bulk-copy gather
-    # over it collapsed transiently in some runs.
-    if args.host_alloc == "huge":  # huge-page, page-locked host store
+    if args.host_alloc == "huge":
         K_h = dd.host_empty((D, B, Hkv, n, d), dt)
         V_h = dd.host_empty((D, B, Hkv, n, d), dt)
     else:
@@ -483,7 +493,8 @@ def run_ours(args, rank, world):
         step(sched_copy)
     torch.cuda.synchronize()
     if args.schedule == "auto":
-        # Calibration: overlap, serial and pipeline in turn, 3 steps each, twice.
+        # Calibration: each two-stream schedule and the serial one in turn,
+        # 3 steps each, twice.
         cands = (("overlap", copy, False, False), ("serial", None, False, False),
                  ("pipeline", copy, True, False), ("guarded", copy, False, True))
         cal = {name: 0.0 for name, _, _, _ in cands}
@@ -508,36 +519,49 @@ def run_ours(args, rank, world):
         _, sched_copy, pipe, guard = cands[names.index(pick)]
         args.schedule_chosen = (f"{pick} (auto; calibration ms per step: "
                                 + ", ".join(f"{k} {v:.2f}" for k, v in cal.items()) + ")")
-    n_serial = max(3, args.steps // 4)
     n_phase = max(3, args.steps // 2)
-    ctx.set_timing_depth(max(args.steps, n_serial, n_phase))
+    ctx.set_timing_depth(max(args.steps, n_phase))
 
-    # Timed region: K overlapped steps, device time on the compute stream.
+    def region(copy_stream, n_steps, timing):
+        """n_steps steps enqueued back to back; device ms on the compute stream."""
+        torch.cuda.synchronize()
+        r0 = torch.cuda.Event(enable_timing=True)
+        r1 = torch.cuda.Event(enable_timing=True)
+        r0.record(compute)
+        for _ in range(n_steps):
+            step(copy_stream, timing=timing)
+        r1.record(compute)
+        torch.cuda.synchronize()
+        return r0.elapsed_time(r1)
+
+    # Timed region: R back-to-back repeats of K steps with events around the
+    # scoring phase only (for the roofline); value is the median repeat.
     clocks = ClockSampler(dev.index)
     time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(compute)
-    for _ in range(args.steps):
-        step(sched_copy, timing="light")  # events around the scoring phase only
-    ev1.record(compute)
-    torch.cuda.synchronize()
-    barrier(world)
+    repeats = max(1, args.repeats)
+    region_ms, score_ms, launches = [], [], 0
+    for _ in range(repeats):
+        barrier(world)
+        region_ms.append(region(sched_copy, args.steps, "light"))
+        barrier(world)
+        timed, sc = recorded(args.steps)
+        score_ms += sc
+        launches = sum(t["launches"] for t in timed)
     clk = clocks.stop()
-    timed, score_ms = recorded(args.steps)
-    launches = sum(t["launches"] for t in timed)
+    region_s = [max_over_ranks(x * 1e-3, world) for x in region_ms]
+    total_s = statistics.median(region_s)
+    value = job_throughput(L, args.steps, total_s, world)
+    values = [job_throughput(L, args.steps, x, world) for x in region_s]
 
-    # The same steps without any per-layer events (only the two around the
-    # region): what the instrumentation of the timed region costs.
-    ev2, ev3 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev2.record(compute)
-    for _ in range(args.steps):
-        step(sched_copy, timing=False)
-    ev3.record(compute)
-    torch.cuda.synchronize()
-    bare_s = max_over_ranks(ev2.elapsed_time(ev3) * 1e-3, world)
-    value_bare = job_throughput(L, args.steps, bare_s, world)
+    # Hidden fraction: the same steps with no per-layer events, overlapped (the
+    # schedule timed above) and serial (one stream), interleaved, 3 each.
+    t_over_l, t_ser_l = [], []
+    for _ in range(3):
+        t_over_l.append(region(sched_copy, args.steps, False) / args.steps)
+        t_ser_l.append(region(None, args.steps, False) / args.steps)
+    t_over, t_ser = statistics.median(t_over_l), statistics.median(t_ser_l)
+    value_bare = job_throughput(L, args.steps, max_over_ranks(t_over * args.steps * 1e-3, world),
+                                world)
 
     # The same steps as one CUDA graph launch each (captured once).
     ctx.capture_step(layers, compute, copy=sched_copy, late_gather=late, pipeline=pipe,
@@ -554,20 +578,17 @@ def run_ours(args, rank, world):
     value_graph = job_throughput(L, args.steps,
                                  max_over_ranks(ev4.elapsed_time(ev5) * 1e-3, world), world)
 
-    # Phase breakdown: the same steps with events around every phase.
+    # Phase breakdown: steps with events around every phase, in the timed
+    # schedule and serially (the serial gather time is the hidden fraction's
+    # denominator).
     for _ in range(n_phase):
         step(sched_copy)
     torch.cuda.synchronize()
     phases, _ = recorded(n_phase)
-    total_s = ev0.elapsed_time(ev1) * 1e-3
-    total_s = max_over_ranks(total_s, world)
-    value = job_throughput(L, args.steps, total_s, world)
-
-    # Serial schedule (same work, one stream) for the hidden fraction.
-    for _ in range(n_serial):
+    for _ in range(n_phase):
         step(None)
     torch.cuda.synchronize()
-    serial, _ = recorded(n_serial)
+    serial, _ = recorded(n_phase)
 
     # End to end through the public API: per step copy every layer's q_spec and q
     # from pinned host memory, run the step, read every layer's output back.
@@ -612,8 +633,6 @@ def run_ours(args, rank, world):
     score_gbs = k_bytes / (score_mean_ms * 1e-3) / 1e9
     gather_ms_layer = statistics.mean(p["gather_ms"] for p in phases) / L
     gather_gbs = g_bytes / (gather_ms_layer * 1e-3) / 1e9
-    t_over = statistics.median(p["step_ms"] for p in phases)
-    t_ser = statistics.median(p["step_ms"] for p in serial)
     g_ser = statistics.median(p["gather_ms"] for p in serial)
     comp_ser = statistics.median(p["score_ms"] + p["topk_ms"] + p["attn_ms"] for p in serial)
     hidden = max(0.0, min(1.0, (t_ser - t_over) / g_ser)) if g_ser > 0 else None
@@ -646,15 +665,24 @@ def run_ours(args, rank, world):
         "host_link_probe_gbs": probe_gbs,
         "gather_alone_gbs": {"bulk_copy": gather_alone[0], "load_store": gather_alone[1]},
         "gather_in_step_gbs": gather_gbs,
+        "value_repeats": values,
+        "value_min": min(values), "value_max": max(values),
+        "value_spread": (max(values) - min(values)) / value,
+        "value_what": f"median of {repeats} back-to-back regions of {args.steps} steps "
+                      "(events around each layer's scoring only)",
         "hidden_fraction": hidden,
+        "hidden_fraction_raw": (t_ser - t_over) / g_ser if g_ser > 0 else None,
+        "hidden_fraction_what": "(serial - overlapped step time) / serial gather time; step "
+                                "times from event-free regions of K steps, 3 of each schedule "
+                                "interleaved (medians); gather time from phase-timed serial steps",
         "hidden_bound": min(1.0, comp_ser / g_ser) if g_ser > 0 else None,
+        "overlapped_step_ms": t_over, "serial_step_ms": t_ser,
+        "serial_gather_ms_per_step": g_ser,
         "phase_ms_per_step": {kk: statistics.mean(p[kk] for p in phases)
                               for kk in ("step_ms", "score_ms", "topk_ms", "gather_ms", "attn_ms")},
-        "serial_step_ms": t_ser,
-        "timed_step_ms_median": statistics.median(p["step_ms"] for p in timed),
         "value_without_layer_events": value_bare,
-        "value_without_layer_events_what": "the same K steps right after the timed region, "
-                                           "with no events inside the steps",
+        "value_without_layer_events_what": "the overlapped event-free regions of the hidden "
+                                           "fraction (median)",
         "value_graph": value_graph,
         "value_graph_what": "the same K steps, each one launch of the step captured as a "
                             "CUDA graph (dd_ctx_capture_step / dd_ctx_replay_step)",

@@ -111,26 +111,31 @@ dd_status dd_check_device(void);
 
 /*
  * Host KV store allocation.  The GPU reads the host store through the host's
- * page tables.  On a Grace host with 64 KiB base pages every scattered row of
- * a cold gather needs its own page translation (about 4 us each), and the
- * thousands in flight also slow the other kernels' memory requests.  Huge
- * pages cut the translations to a handful per layer.  dd_host_alloc maps
+ * page tables.  On a Grace host with 64 KiB base pages a long-context gather
+ * touches hundreds of thousands of distinct pages per layer, each needing its
+ * own translation; the translations slow the gather and the kernels running
+ * beside it.  Huge pages cut them to a handful per layer.  dd_host_alloc maps
  * `bytes` (rounded up to whole huge pages) of anonymous memory aligned to the
  * host's huge-page size, asks for transparent huge pages (madvise), faults it
- * in from the CPU (several threads; the pages read as zero), and page-locks
- * and maps it for the GPU (cudaHostRegister).  The caller owns the memory and
- * releases it with dd_host_free.  Returns DD_ERR_OOM if the mapping fails and
- * DD_ERR_CUDA if registration fails.  Any page-locked memory works with the
- * gather.
- * Measured on GB300 with 512 MiB huge pages, on the 7B-32K workload (8 layer
- * slots cycled): most runs gathered at warm-translation speed, but in some
- * runs the bulk-copy gather (mode 0) over such a store collapsed for a while,
- * so the benchmark keeps plain page-locked memory as its default.
+ * in from the CPU (several threads; the pages read as zero), locks it (mlock,
+ * best effort: dd_host_store_locked reports whether it held) and registers it
+ * with CUDA (cudaHostRegister).  The caller owns the memory, fills it from the
+ * CPU and releases it with dd_host_free.  Returns DD_ERR_OOM if the mapping
+ * fails and DD_ERR_CUDA if registration fails.  Any page-locked memory works
+ * with the gather.
+ * Measured on GB300 (512 MiB huge pages, a 64 GiB store filled by the CPU and
+ * cycled by gathers): locked, the gather held 183-188 GB/s; registered but not
+ * locked, the host split some huge pages and migrated pages once the GPU
+ * started reading, and gathers fell to 1-3 GB/s for the rest of the run.
  */
 dd_status dd_host_alloc(size_t bytes, void** out);
-/* Unregister and unmap a region from dd_host_alloc (NULL is a no-op);
- * DD_ERR_INVALID_ARG for any other pointer. */
+/* Unlock, unregister and unmap a region from dd_host_alloc (NULL is a
+ * no-op); DD_ERR_INVALID_ARG for any other pointer. */
 dd_status dd_host_free(void* p);
+/* 1 if p lies in a store from dd_host_alloc, else 0. */
+int dd_host_store_kind(const void* p);
+/* 1 if p lies in a store from dd_host_alloc whose pages are locked, else 0. */
+int dd_host_store_locked(const void* p);
 /* The host huge-page size the allocator and the gather's translation
  * prefetch use (transparent-huge-page size, else 2 MiB). */
 size_t dd_host_page_bytes(void);
@@ -185,6 +190,20 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
 dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v_host,
                         const int32_t* idx, void* k_buf, void* v_buf, int mode,
                         dd_stream_t stream);
+
+/*
+ * Geometry of the bulk-copy gather (mode 0) for every later launch in the
+ * process, by dd_gather_h2d and dd_decode_step alike: grid_pct one-warp CTAs
+ * per 100 SMs (1..800), tile_bytes of rows per tensor and shared-memory stage
+ * (a multiple of 512, 512..16384; rows wider than a tile move one per stage),
+ * and `stages` stages per CTA (1..8), with 2 * stages * tile_bytes at most
+ * 227 KiB of shared memory.  Rows in flight are the CTAs times the
+ * stages times the rows of a tile.  The default, (100, 4096, 3), puts one
+ * 24 KiB CTA on each SM, which fits beside three scoring CTAs.  Launches
+ * already enqueued keep the geometry they had.  DD_ERR_INVALID_ARG outside
+ * the ranges.  The bytes gathered never depend on it.
+ */
+dd_status dd_set_gather_geometry(int grid_pct, int tile_bytes, int stages);
 
 /*
  * Step 4 for one layer: out[b,h] = sum_{j in S} softmax_S(q[b,h] . K_j /

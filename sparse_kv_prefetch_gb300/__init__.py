@@ -114,7 +114,10 @@ def _lib():
             "dd_host_alloc": ([ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)], ctypes.c_int),
             "dd_host_free": ([ctypes.c_void_p], ctypes.c_int),
             "dd_host_page_bytes": ([], ctypes.c_size_t),
+            "dd_host_store_kind": ([ctypes.c_void_p], ctypes.c_int),
+            "dd_host_store_locked": ([ctypes.c_void_p], ctypes.c_int),
             "dd_workspace_size": ([S, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+            "dd_set_gather_geometry": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_int),
             "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dd_gather_h2d": ([S, P, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
             "dd_sparse_decode_attn": ([S, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
@@ -178,13 +181,14 @@ def _dev(x) -> Optional[int]:
 
 
 def _host(x) -> Optional[int]:
-    """Address of a page-locked host buffer (pinned CPU tensor or raw int)."""
+    """Address of a page-locked host buffer (pinned CPU tensor, a tensor from
+    host_empty, or raw int)."""
     if x is None or isinstance(x, int):
         return x
     if x.is_cuda or not x.is_contiguous():
         raise TypeError("expected a contiguous CPU tensor")
-    if not x.is_pinned():
-        raise ValueError("the host KV store must be page-locked (pin_memory=True)")
+    if not x.is_pinned() and not _lib().dd_host_store_kind(x.data_ptr()):
+        raise ValueError("the host KV store must be page-locked (pin_memory=True or host_empty)")
     return x.data_ptr()
 
 
@@ -202,9 +206,9 @@ def version() -> int:
 
 
 def host_empty(shape, dtype):
-    """An uninitialised CPU tensor in a huge-page, page-locked host region from
-    dd_host_alloc (the recommended host KV store); freed with dd_host_free when
-    the tensor and all its views are gone."""
+    """An uninitialised CPU tensor in a locked, page-locked huge-page host
+    region from dd_host_alloc (the recommended host KV store); freed with
+    dd_host_free when the tensor and all its views are gone."""
     import weakref
 
     import torch
@@ -224,6 +228,11 @@ def host_page_bytes() -> int:
     return _lib().dd_host_page_bytes()
 
 
+def host_store_locked(t) -> bool:
+    """True if the tensor lies in a dd_host_alloc store whose pages are locked."""
+    return bool(_lib().dd_host_store_locked(t.data_ptr()))
+
+
 def debug_expire_wait(limit_ns: int, stream=None):
     """Test hook: a device wait that nothing completes gives up after limit_ns;
     the next check_device raises DD_ERR_TIMEOUT (see dd.h)."""
@@ -233,6 +242,11 @@ def debug_expire_wait(limit_ns: int, stream=None):
 def check_device():
     """Raise DDError(DD_ERR_TIMEOUT) if a bounded device-side wait gave up."""
     _check(_lib().dd_check_device(), "dd_check_device")
+
+
+def set_gather_geometry(grid_pct: int = 100, tile_bytes: int = 4096, stages: int = 3):
+    """Geometry of the bulk-copy gather for later launches (see dd.h)."""
+    _check(_lib().dd_set_gather_geometry(grid_pct, tile_bytes, stages), "dd_set_gather_geometry")
 
 
 def workspace_size(shape: Shape) -> int:

@@ -19,7 +19,7 @@ OUT = os.path.join(HERE, "libdd.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
 
 SOURCES = ["api.cu", "score.cu", "topk.cu", "gather.cu", "attn.cu", "correct.cu", "noalloc.cu",
-           "landmark.cu", "debug.cu"]
+           "landmark.cu", "debug.cu", "hoststore.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
                      "-I", INCLUDE, "-I", CSRC]
@@ -32,8 +32,8 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, extra: list[str], bdir: str = BUILD_DIR) -> str:
+    obj = os.path.join(bdir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *NVCC_FLAGS, *extra, "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -43,11 +43,17 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False, out: str = OUT) -> str:
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(verbose_ptxas: bool = False, out: str = OUT, defines=()) -> str:
+    """Compile and link libdd.so into `out`.  `defines` are extra -D macros
+    (compile-time geometry of the kernels, e.g. "DD_GATHER_STAGES=4"); a build
+    with defines goes to its own object folder."""
+    bdir = BUILD_DIR if not defines else os.path.join(
+        BUILD_DIR, "_".join(d.replace("=", "-") for d in defines))
+    os.makedirs(bdir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    extra += [f"-D{d}" for d in defines]
     with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), SOURCES))
+        objs = list(ex.map(lambda s: _compile(s, extra, bdir), SOURCES))
     tmp = out + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-cudart", "shared", "-o", tmp, *objs,
            "-Xlinker", "-rpath=/usr/local/cuda/lib64"]

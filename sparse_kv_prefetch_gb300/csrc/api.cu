@@ -9,8 +9,6 @@
 #include <stdlib.h>
 #include <string.h>
 
-#include <sys/mman.h>
-
 #include <algorithm>
 
 #include <cstdio>
@@ -20,10 +18,6 @@
 #include <new>
 #include <thread>
 #include <vector>
-
-#ifndef DD_HOST_PREFAULT
-#define DD_HOST_PREFAULT 1
-#endif
 
 #include "dd_internal.cuh"
 
@@ -83,20 +77,6 @@ dd_status resolve(const dd_shape* s, Dims* o) {
   if ((long long)d.U * d.k > 0x7FFFFFFFLL) return DD_ERR_UNSUPPORTED;
   *o = d;
   return DD_OK;
-}
-
-size_t host_page_bytes() {
-  static size_t cached = 0;
-  if (cached) return cached;
-  size_t v = 0;
-  if (FILE* f = std::fopen("/sys/kernel/mm/transparent_hugepage/hpage_pmd_size", "r")) {
-    unsigned long long x = 0;
-    if (std::fscanf(f, "%llu", &x) == 1) v = (size_t)x;
-    std::fclose(f);
-  }
-  if (v < 4096 || (v & (v - 1))) v = (size_t)2 << 20;
-  cached = v;
-  return v;
 }
 
 WsLayout ws_layout(const Dims& d) {
@@ -162,18 +142,7 @@ dd_status resolve_landmarks(const dd_shape* s, int chunk, LandmarkDims* out) {
   return DD_OK;
 }
 
-}  // namespace dd
-
-using namespace dd;
-
-namespace {
-
-bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
-
-dd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DD_OK : DD_ERR_CUDA; }
-
-// True if p is device (or managed) memory of the current CUDA context.
-// Device memory of the current device (or managed memory).
+// Device memory of the current device, or managed memory.
 bool is_device_ptr(const void* p) {
   cudaPointerAttributes a;
   if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
@@ -191,17 +160,15 @@ bool all_device(std::initializer_list<const void*> ps) {
   return true;
 }
 
-// Device-accessible address of a page-locked host pointer; NULL if the
-// pointer is not page-locked host memory known to CUDA.
-const void* host_to_device(const void* p) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();  // clear the non-sticky error
-    return nullptr;
-  }
-  if (a.type != cudaMemoryTypeHost) return nullptr;
-  return a.devicePointer;
-}
+}  // namespace dd
+
+using namespace dd;
+
+namespace {
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+dd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DD_OK : DD_ERR_CUDA; }
 
 }  // namespace
 
@@ -221,92 +188,6 @@ const char* dd_status_string(int s) {
 
 int dd_version(void) { return DD_VERSION; }
 
-// ------------------------------------------------------------ host store
-
-namespace {
-std::mutex g_host_mu;
-std::map<void*, size_t> g_host_regions;  // dd_host_alloc base -> mapped bytes
-}  // namespace
-
-}  // extern "C"
-
-namespace dd {
-bool in_huge_page_store(const void* p) {
-  std::lock_guard<std::mutex> lock(g_host_mu);
-  auto it = g_host_regions.upper_bound(const_cast<void*>(p));
-  if (it == g_host_regions.begin()) return false;
-  --it;
-  const uintptr_t base = (uintptr_t)it->first, q = (uintptr_t)p;
-  return q >= base && q < base + it->second;
-}
-}  // namespace dd
-
-extern "C" {
-
-dd_status dd_host_alloc(size_t bytes, void** out) {
-  if (!out || bytes == 0) return DD_ERR_INVALID_ARG;
-  *out = nullptr;
-  const size_t page = host_page_bytes();
-  const size_t len = (bytes + page - 1) / page * page;
-  // Over-map by one huge page so the region can start on a huge-page boundary.
-  void* raw = mmap(nullptr, len + page, PROT_READ | PROT_WRITE, MAP_PRIVATE | MAP_ANONYMOUS, -1, 0);
-  if (raw == MAP_FAILED) return DD_ERR_OOM;
-  const uintptr_t r = (uintptr_t)raw;
-  const uintptr_t base = (r + page - 1) / page * page;
-  if (base > r) munmap(raw, base - r);
-  const uintptr_t tail = base + len, raw_end = r + len + page;
-  if (raw_end > tail) munmap((void*)tail, raw_end - tail);
-  void* p = (void*)base;
-  madvise(p, len, MADV_HUGEPAGE);  // advisory: huge pages where the host allows them
-#if DD_HOST_PREFAULT
-  // Fault the region in from the CPU (one store per 64 KiB, several threads,
-  // each on its own huge pages) before registering it, so that the kernel
-  // backs it with huge pages at first touch.
-  {
-    const unsigned hw = std::thread::hardware_concurrency();
-    const size_t n_pages = len / page;
-    const unsigned n_thr = (unsigned)std::min<size_t>(n_pages, hw ? std::min(hw, 16u) : 4u);
-    auto fault = [&](unsigned t) {
-      for (size_t pg = t; pg < n_pages; pg += n_thr)
-        for (size_t off = 0; off < page; off += 65536)
-          static_cast<volatile unsigned char*>(p)[pg * page + off] = 0;
-    };
-    std::vector<std::thread> th;
-    for (unsigned t = 1; t < n_thr; ++t) th.emplace_back(fault, t);
-    fault(0);
-    for (auto& x : th) x.join();
-  }
-#endif
-  if (cudaHostRegister(p, len, cudaHostRegisterDefault) != cudaSuccess) {
-    cudaGetLastError();
-    munmap(p, len);
-    return DD_ERR_CUDA;
-  }
-  {
-    std::lock_guard<std::mutex> lock(g_host_mu);
-    g_host_regions[p] = len;
-  }
-  *out = p;
-  return DD_OK;
-}
-
-dd_status dd_host_free(void* p) {
-  if (!p) return DD_OK;
-  size_t len = 0;
-  {
-    std::lock_guard<std::mutex> lock(g_host_mu);
-    auto it = g_host_regions.find(p);
-    if (it == g_host_regions.end()) return DD_ERR_INVALID_ARG;
-    len = it->second;
-    g_host_regions.erase(it);
-  }
-  const cudaError_t e = cudaHostUnregister(p);
-  munmap(p, len);
-  return e == cudaSuccess ? DD_OK : DD_ERR_CUDA;
-}
-
-size_t dd_host_page_bytes(void) { return host_page_bytes(); }
-
 dd_status dd_check_device(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return DD_ERR_CUDA;
   const unsigned int a = take_score_status();
@@ -318,6 +199,10 @@ dd_status dd_check_device(void) {
 dd_status dd_debug_expire_wait(uint64_t limit_ns, dd_stream_t stream) {
   if (limit_ns == 0 || limit_ns > 100000000ull) return DD_ERR_INVALID_ARG;
   return cuda_status(launch_expire_wait(limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dd_status dd_set_gather_geometry(int grid_pct, int tile_bytes, int stages) {
+  return set_gather_geometry(grid_pct, tile_bytes, stages);
 }
 
 dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes) {

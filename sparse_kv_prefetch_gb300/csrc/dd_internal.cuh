@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <initializer_list>
+
 #include "dd.h"
 
 namespace dd {
@@ -52,8 +54,21 @@ cudaError_t launch_score_select(const Dims& d, const void* q_spec, const void* k
 cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
                           const int32_t* idx, void* k_buf, void* v_buf, int mode,
                           cudaStream_t st, bool touch);
-// True if p lies in a host store allocated by dd_host_alloc.
+// Geometry of the bulk-copy gather (mode 0), process-wide: grid in percent
+// of the SM count, bytes per tensor of a shared-memory stage, stages per CTA.
+dd_status set_gather_geometry(int grid_pct, int tile_bytes, int stages);
+// Host stores allocated by the library (hoststore.cu).
+// True if p lies in a store from dd_host_alloc (transparent huge pages,
+// registered with CUDA), whose translations the gather prefetches.
 bool in_huge_page_store(const void* p);
+// Device-accessible address of page-locked host memory known to CUDA (a
+// host KV store); NULL otherwise.
+const void* host_to_device(const void* p);
+
+// Pointer checks of the C ABI (api.cu): device memory of the current device,
+// or managed memory; all_device accepts NULL entries.
+bool is_device_ptr(const void* p);
+bool all_device(std::initializer_list<const void*> ps);
 // Where the attention reads the window's keys: row off + i (i < W) of each
 // unit's `stride` rows starting at p.
 struct WindowK {
@@ -240,6 +255,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that lets the thread sleep up to hint_ns while the phase is
+// incomplete (it consumes no issue slots meanwhile).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t global_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
@@ -257,6 +285,15 @@ __device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, ui
 }
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return mbar_wait_for(bar, parity, kWaitLimitNs);
+}
+// mbar_wait for long waits (host-memory copies): sleeps between polls.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                uint32_t hint_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_sleep(bar, parity, hint_ns))
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  return true;
 }
 // global -> shared, completion counted on `bar` (bytes and addresses 16-aligned).
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gmem_src, uint32_t bytes,

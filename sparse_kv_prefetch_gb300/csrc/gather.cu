@@ -20,12 +20,10 @@
 // mode 1, gather_lsu_kernel: every thread keeps kInFlight 16-byte loads from
 //   host memory outstanding (consecutive threads read consecutive 16-byte
 //   pieces of a row).  Kept as the plain reference design.
-#include "dd_internal.cuh"
+#include <algorithm>
+#include <atomic>
 
-// Grid of the bulk-copy gather, in percent of the SM count.
-#ifndef DD_GATHER_GRID_PCT
-#define DD_GATHER_GRID_PCT 200
-#endif
+#include "dd_internal.cuh"
 
 namespace dd {
 namespace {
@@ -64,27 +62,44 @@ __global__ void __launch_bounds__(32)
 __device__ unsigned int g_touch_sink = 0;
 
 // ------------------------------------------------------------ mode 0 (TMA)
-constexpr int kTileBytes = 8192;  // per tensor per stage
-constexpr int kTmaStages = 4;
-constexpr size_t kTmaSmem = (size_t)2 * kTmaStages * kTileBytes + kTmaStages * sizeof(uint64_t);
+//
+// Geometry of a launch: `ctas` one-warp CTAs, each with `stages` shared-memory
+// stages of R rows per tensor (R = tile bytes / row bytes).  Rows in flight
+// are ctas * stages * R per tensor; the default (one CTA per SM, 3 stages of
+// 4 KiB) needs 24 KiB of shared memory per CTA, which fits beside three
+// scoring CTAs on an SM.  dd_set_gather_geometry changes it process-wide.
+#ifndef DD_GATHER_WAIT_HINT_NS
+#define DD_GATHER_WAIT_HINT_NS 0
+#endif
+#ifndef DD_GATHER_HOST_EVICT_FIRST
+#define DD_GATHER_HOST_EVICT_FIRST 0
+#endif
+constexpr int kMaxStages = 8;
+constexpr int kMaxTileBytes = 16384;
+constexpr int kMaxDynSmem = 227 * 1024;  // largest opt-in per CTA
+std::atomic<int> g_grid_pct{100}, g_tile_bytes{4096}, g_stages{3};
+
+size_t tma_smem(int rows, int rb, int stages) {
+  return (size_t)2 * stages * rows * rb + (size_t)stages * sizeof(uint64_t);
+}
 
 template <int RB>  // bytes per row
 __global__ void __launch_bounds__(32)
     gather_tma_kernel(const unsigned char* __restrict__ k_host,
                       const unsigned char* __restrict__ v_host, const int32_t* __restrict__ idx,
                       unsigned char* __restrict__ k_buf, unsigned char* __restrict__ v_buf, int n,
-                      int k, int units) {
-  constexpr int R = kTileBytes / RB;  // rows per tile
+                      int k, int units, int R, int stages) {
   extern __shared__ __align__(128) unsigned char smem[];
+  const int tile_bytes = R * RB;
   unsigned char* ring_k = smem;
-  unsigned char* ring_v = smem + (size_t)kTmaStages * kTileBytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)2 * kTmaStages * kTileBytes);
+  unsigned char* ring_v = smem + (size_t)stages * tile_bytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)2 * stages * tile_bytes);
   const int lane = threadIdx.x;
   const int tiles_per_unit = (k + R - 1) / R;
   const int n_tiles = units * tiles_per_unit;
 
   if (lane == 0) {
-    for (int s = 0; s < kTmaStages; ++s) mbar_init(&full[s], 1);
+    for (int s = 0; s < stages; ++s) mbar_init(&full[s], 1);
     mbar_fence_init();
   }
   __syncwarp();
@@ -111,21 +126,34 @@ __global__ void __launch_bounds__(32)
         const int len = __ffs(~after);  // this row plus the continuing rows after it
         const size_t src = ((size_t)u * n + j) * RB;
         const uint32_t bytes = (uint32_t)(len * RB);
-        bulk_load(ring_k + (size_t)s * kTileBytes + (size_t)r * RB, k_host + src, bytes, &full[s]);
-        bulk_load(ring_v + (size_t)s * kTileBytes + (size_t)r * RB, v_host + src, bytes, &full[s]);
+#if DD_GATHER_HOST_EVICT_FIRST
+        const uint64_t pol = l2_evict_first_policy();
+        bulk_load_hint(ring_k + (size_t)s * tile_bytes + (size_t)r * RB, k_host + src, bytes,
+                       &full[s], pol);
+        bulk_load_hint(ring_v + (size_t)s * tile_bytes + (size_t)r * RB, v_host + src, bytes,
+                       &full[s], pol);
+#else
+        bulk_load(ring_k + (size_t)s * tile_bytes + (size_t)r * RB, k_host + src, bytes, &full[s]);
+        bulk_load(ring_v + (size_t)s * tile_bytes + (size_t)r * RB, v_host + src, bytes, &full[s]);
+#endif
       }
     }
   };
 
-  for (int p = 0; p < kTmaStages; ++p) {
+  for (int p = 0; p < stages; ++p) {
     const int t = blockIdx.x + p * gridDim.x;
     if (t < n_tiles) issue(t, p);
   }
   bool ok = true;
   int it = 0;
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
-    const int s = it % kTmaStages;
-    if (!mbar_wait(&full[s], (it / kTmaStages) & 1)) {
+    const int s = it % stages;
+#if DD_GATHER_WAIT_HINT_NS
+    const bool landed = mbar_wait_sleep(&full[s], (it / stages) & 1, DD_GATHER_WAIT_HINT_NS);
+#else
+    const bool landed = mbar_wait(&full[s], (it / stages) & 1);
+#endif
+    if (!landed) {
       ok = false;
       break;
     }
@@ -133,19 +161,19 @@ __global__ void __launch_bounds__(32)
       const int u = t / tiles_per_unit, i0 = (t - u * tiles_per_unit) * R;
       const int nr = min(R, k - i0);
       const size_t dst = ((size_t)u * k + i0) * RB;
-      bulk_store(k_buf + dst, ring_k + (size_t)s * kTileBytes, (uint32_t)(nr * RB));
-      bulk_store(v_buf + dst, ring_v + (size_t)s * kTileBytes, (uint32_t)(nr * RB));
+      bulk_store(k_buf + dst, ring_k + (size_t)s * tile_bytes, (uint32_t)(nr * RB));
+      bulk_store(v_buf + dst, ring_v + (size_t)s * tile_bytes, (uint32_t)(nr * RB));
       bulk_commit();
       bulk_wait_read_all();  // the stage may be refilled once the stores have read it
     }
     __syncwarp();
-    const int nt = t + kTmaStages * gridDim.x;
+    const int nt = t + stages * gridDim.x;
     if (nt < n_tiles) issue(nt, s);
   }
   if (!ok) {
     if (lane == 0) atomicOr(&g_gather_status, 1u);
     // let the copies still in flight land before the CTA exits
-    for (int s = 0; s < kTmaStages; ++s) {
+    for (int s = 0; s < stages; ++s) {
       mbar_wait(&full[s], 0);
       mbar_wait(&full[s], 1);
     }
@@ -157,16 +185,18 @@ template <int RB>
 cudaError_t launch_tma(const Dims& d, const void* kh, const void* vh, const int32_t* idx,
                        void* kb, void* vb, cudaStream_t st) {
   static unsigned long long prepared = 0;
-  cudaError_t e = prepare_kernel(gather_tma_kernel<RB>, &prepared, (int)kTmaSmem);
+  cudaError_t e = prepare_kernel(gather_tma_kernel<RB>, &prepared, kMaxDynSmem);
   if (e != cudaSuccess) return e;
-  constexpr int R = kTileBytes / RB;
+  const int R = std::max(1, std::min(64, g_tile_bytes.load() / RB));
+  const int stages = g_stages.load();
   const long long tiles = (long long)d.U * ((d.k + R - 1) / R);
-  long long grid = (long long)sm_count() * DD_GATHER_GRID_PCT / 100;
+  long long grid = ((long long)sm_count() * g_grid_pct.load() + 99) / 100;
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
-  gather_tma_kernel<RB><<<(unsigned)grid, 32, kTmaSmem, st>>>(
+  gather_tma_kernel<RB><<<(unsigned)grid, 32, tma_smem(R, RB, stages), st>>>(
       static_cast<const unsigned char*>(kh), static_cast<const unsigned char*>(vh), idx,
-      static_cast<unsigned char*>(kb), static_cast<unsigned char*>(vb), d.n, d.k, d.U);
+      static_cast<unsigned char*>(kb), static_cast<unsigned char*>(vb), d.n, d.k, d.U, R,
+      stages);
   return cudaGetLastError();
 }
 
@@ -267,6 +297,17 @@ cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
     }
   }
   return cudaErrorInvalidValue;
+}
+
+dd_status set_gather_geometry(int grid_pct, int tile_bytes, int stages) {
+  if (grid_pct < 1 || grid_pct > 800 || stages < 1 || stages > kMaxStages ||
+      tile_bytes < 512 || tile_bytes > kMaxTileBytes || tile_bytes % 512 != 0 ||
+      tma_smem(1, tile_bytes, stages) > (size_t)kMaxDynSmem)
+    return DD_ERR_INVALID_ARG;
+  g_grid_pct.store(grid_pct);
+  g_tile_bytes.store(tile_bytes);
+  g_stages.store(stages);
+  return DD_OK;
 }
 
 unsigned int take_gather_status() {

@@ -58,15 +58,6 @@ dd_status scratch_address(void** out) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-bool device_ptr(const void* p) {
-  cudaPointerAttributes a;
-  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
-    cudaGetLastError();
-    return false;
-  }
-  return a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged;
-}
-
 }  // namespace
 
 extern "C" dd_status dd_sparse_decode_attn_noalloc(const dd_shape* shape, const void* q,
@@ -86,8 +77,10 @@ extern "C" dd_status dd_sparse_decode_attn_noalloc(const dd_shape* shape, const 
   if (!aligned16(q) || !aligned16(k_buf) || !aligned16(v_buf) || !aligned16(k_dev) ||
       !aligned16(out) || (v_win && !aligned16(v_win)))
     return DD_ERR_INVALID_ARG;
-  for (const void* p : {q, k_buf, v_buf, k_dev, v_win, static_cast<const void*>(out)})
-    if (p && !device_ptr(p)) return DD_ERR_INVALID_ARG;
+  // The same pointer check as every other entry point: device memory of the
+  // current device (or managed memory).
+  if (!dd::all_device({q, k_buf, v_buf, k_dev, v_win, static_cast<const void*>(out)}))
+    return DD_ERR_INVALID_ARG;
   void* base = nullptr;
   st = scratch_address(&base);
   if (st != DD_OK) return st;

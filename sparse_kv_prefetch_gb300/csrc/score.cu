@@ -61,10 +61,19 @@ constexpr int kSelWarps = kConsumerWarps;
 constexpr int kSelCap = 1024;  // list entries per warp
 using SelSmem = sel::Smem<kSelWarps, kSelCap>;
 constexpr size_t kRingBytes = (size_t)kStages * kStageBytes;
-constexpr size_t kRegionBytes =
-    ((kRingBytes > sizeof(SelSmem) ? kRingBytes : sizeof(SelSmem)) + 127) / 128 * 128;
-// [0, kRegionBytes): the ring, later the selection's lists; then the mbarriers.
-constexpr size_t kScoreSmem = kRegionBytes + 2 * kStages * sizeof(uint64_t);
+// Dynamic shared memory: [0, region): the ring (and, when FUSED, later the
+// selection's lists, which need more); then the mbarriers.  The plain kernel
+// asks only for the ring, so that three of its CTAs leave room on an SM for a
+// gather CTA running beside them.
+template <bool FUSED>
+__host__ __device__ constexpr size_t region_bytes() {
+  return ((FUSED && sizeof(SelSmem) > kRingBytes ? sizeof(SelSmem) : kRingBytes) + 127) / 128 *
+         128;
+}
+template <bool FUSED>
+__host__ __device__ constexpr size_t score_smem() {
+  return region_bytes<FUSED>() + 2 * kStages * sizeof(uint64_t);
+}
 
 // Selection outputs of the fused kernel (unused when FUSED is false).
 struct FusedOut {
@@ -92,7 +101,7 @@ __global__ void __launch_bounds__(kScoreThreads)
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kRegionBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + region_bytes<FUSED>());
   uint64_t* empty = full + kStages;
 
   const int item = blockIdx.x;
@@ -140,10 +149,28 @@ __global__ void __launch_bounds__(kScoreThreads)
   } else {
     const int sub = lane % LPR;
     const int grp = warp * RPW + lane / LPR;
+    // The lane's partial sums live in acc[N], N = G * RPG values (head g,
+    // stage row slot i).  The transposed reduction below halves them S times,
+    // each time keeping the lower half of the slots and sending the upper
+    // half to the lane 2^t away.  For that to need no selects, each lane
+    // stores value v in slot v ^ X: X has, at bit LOGN-1-t, bit t of `sub`,
+    // so at step t the lane keeps exactly the values its side of the pair
+    // owns.  The permutation costs nothing inside the loop: slot (g, i) is
+    // computed from head g ^ Xg (the query is loaded permuted) and stage row
+    // i ^ Xi (a per-lane shared-memory offset).  After the S steps, lane
+    // `sub` holds the totals of the P values X + p (p < P); X = prefix * P
+    // where prefix is `sub`'s low S bits reversed.  Only lanes with
+    // sub < 2^S hold distinct values, and all of one lane's values belong to
+    // the same head g_lane.
+    constexpr int LOGN = ilog2(N);
+    int X = 0;
+#pragma unroll
+    for (int t = 0; t < S; ++t) X |= ((sub >> t) & 1) << (LOGN - 1 - t);
+    const int Xg = X / RPG, Xi = X % RPG;
     float qf[G][VEC];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const size_t piece = (size_t)(b * Hq + hk * G + g) * LPR + sub;
+      const size_t piece = (size_t)(b * Hq + hk * G + (g ^ Xg)) * LPR + sub;
       if constexpr (QB) {
         static_assert(VEC == 4, "a bf16 query widens to fp32 keys only");
         const uint2 v = __ldg(reinterpret_cast<const uint2*>(q_spec) + piece);
@@ -155,16 +182,13 @@ __global__ void __launch_bounds__(kScoreThreads)
         unpack(ld_ro(q_spec + piece), qf[g]);
       }
     }
-
-    // After the transposed reduction below, lane `sub` holds the totals of
-    // the P values with indices prefix*P + p (p < P), index = g*RPG + i for
-    // head g and stage row i; prefix is `sub`'s low S bits reversed.  Only
-    // lanes with sub < 2^S hold distinct values, and all of one lane's values
-    // belong to the same head g_lane.
-    int prefix = 0;
+    // Shared-memory offset (in 16-byte pieces) of the row in slot i.
+    int row_off[RPG];
 #pragma unroll
-    for (int t = 0; t < S; ++t) prefix |= ((sub >> t) & 1) << (S - 1 - t);
-    const int g_lane = (prefix * P) / RPG;
+    for (int i = 0; i < RPG; ++i) row_off[i] = ((i ^ Xi) * NG + grp) * LPR + sub;
+
+    const int prefix = X / P;
+    const int g_lane = X / RPG;
     const bool writer = (sub >> S) == 0;
     if (writer) head = g_lane;
     float* lg_row = logits + (size_t)(b * Hq + hk * G + g_lane) * ldn;
@@ -177,38 +201,42 @@ __global__ void __launch_bounds__(kScoreThreads)
       }
       const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * kStageBytes);
       const int r0 = j_begin + t * SR;
-      // Row (i * NG + grp) of the stage, for i < RPG, belongs to this lane group.
+      // Stage row (i * NG + grp), for i < RPG, belongs to this lane group.
       float acc[N];
+      static_assert(RPG % 2 == 0, "rows are summed in pairs");
 #pragma unroll
-      for (int i = 0; i < RPG; ++i) {
-        float kf[VEC];
-        unpack(st[(size_t)(i * NG + grp) * LPR + sub], kf);
+      for (int i = 0; i < RPG; i += 2) {
+        float k0[VEC], k1[VEC];
+        unpack(st[row_off[i]], k0);
+        unpack(st[row_off[i + 1]], k1);
         // Packed fp32 FMA (two lanes of arithmetic per instruction): the even
-        // and the odd elements accumulate separately and are added at the end.
+        // and the odd elements accumulate separately; one packed add then
+        // finishes two rows' dot products.
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          float2 a = make_float2(0.f, 0.f);
+          float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int e = 0; e < VEC; e += 2)
-            a = __ffma2_rn(make_float2(qf[g][e], qf[g][e + 1]), make_float2(kf[e], kf[e + 1]), a);
-          acc[g * RPG + i] = a.x + a.y;
+          for (int e = 0; e < VEC; e += 2) {
+            const float2 qv = make_float2(qf[g][e], qf[g][e + 1]);
+            a0 = __ffma2_rn(qv, make_float2(k0[e], k0[e + 1]), a0);
+            a1 = __ffma2_rn(qv, make_float2(k1[e], k1[e + 1]), a1);
+          }
+          const float2 sum = __fadd2_rn(make_float2(a0.x, a1.x), make_float2(a0.y, a1.y));
+          acc[g * RPG + i] = sum.x;
+          acc[g * RPG + i + 1] = sum.y;
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
       // Transposed reduction over the LPR lanes of the group: at step t each
-      // lane keeps one half of its values, sends the other half to the lane
-      // 2^t away and adds what it receives, so the number of values halves.
+      // lane keeps the lower half of its slots, sends the upper half to the
+      // lane 2^t away and adds what it receives.
 #pragma unroll
       for (int t2 = 0; t2 < S; ++t2) {
         const int half = (N >> t2) / 2;
-        const bool up = (sub >> t2) & 1;
 #pragma unroll
-        for (int i = 0; i < half; ++i) {
-          const float send = up ? acc[i] : acc[i + half];
-          const float keep = up ? acc[i + half] : acc[i];
-          acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, 1 << t2);
-        }
+        for (int i = 0; i < half; ++i)
+          acc[i] = acc[i] + __shfl_xor_sync(0xffffffffu, acc[i + half], 1 << t2);
       }
       // Remaining lane bits: plain butterfly on the P values left.
 #pragma unroll
@@ -223,9 +251,12 @@ __global__ void __launch_bounds__(kScoreThreads)
           if (j < j_end) {
             const float sv = acc[p] * scale;
             lg_row[j] = sv;
-            const float m_new = fmaxf(m_run, sv);
-            l_run = l_run * __expf(m_run - m_new) + __expf(sv - m_new);
-            m_run = m_new;
+            // Online (max, sum of exp) with one exponential: a new maximum
+            // rescales the sum, any other logit adds its term.
+            const float dv = sv - m_run;
+            const float ev = __expf(-fabsf(dv));
+            l_run = dv > 0.f ? fmaf(l_run, ev, 1.f) : l_run + ev;
+            m_run = fmaxf(m_run, sv);
           }
         }
       }
@@ -289,11 +320,12 @@ template <typename T, int D, int G, bool FUSED, bool QB = false>
 cudaError_t launch_typed(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
                          float2* part, const FusedOut& fo, cudaStream_t st) {
   static unsigned long long prepared = 0;
-  cudaError_t e = prepare_kernel(score_kernel<T, D, G, FUSED, QB>, &prepared, (int)kScoreSmem);
+  constexpr size_t smem_bytes = score_smem<FUSED>();
+  cudaError_t e = prepare_kernel(score_kernel<T, D, G, FUSED, QB>, &prepared, (int)smem_bytes);
   if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)d.d);
   const unsigned grid = (unsigned)d.U * (unsigned)d.nchunks;
-  score_kernel<T, D, G, FUSED, QB><<<grid, kScoreThreads, kScoreSmem, st>>>(
+  score_kernel<T, D, G, FUSED, QB><<<grid, kScoreThreads, smem_bytes, st>>>(
       static_cast<const uint4*>(q_spec), static_cast<const unsigned char*>(k_dev), logits, part,
       d.n, d.ldn, d.Hq, d.Hkv, d.chunk, d.nchunks, scale, fo);
   return cudaGetLastError();

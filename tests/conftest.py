@@ -32,3 +32,22 @@ def _built_library():
     """Compile libdd.so (nvcc, sm_103a) if it is missing or stale."""
     from sparse_kv_prefetch_gb300 import build
     build.ensure_built()
+
+
+@pytest.fixture(autouse=True)
+def _release_memory(request):
+    """After every GPU test: free cached device memory and the page-locked host
+    blocks torch keeps for reuse, so the full-size cases (host stores of up to
+    96 GiB) never add up on the host."""
+    yield
+    if "gpu" not in request.keywords:
+        return
+    import gc
+
+    import torch
+    gc.collect()
+    if torch.cuda.is_available() and torch.cuda.is_initialized():
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        if hasattr(torch._C, "_host_emptyCache"):
+            torch._C._host_emptyCache()

@@ -42,8 +42,12 @@ SMALL = {
 
 
 def _free():
+    """Release device memory and the page-locked host blocks torch keeps
+    cached, so that full-size cases do not add up on the host."""
     gc.collect()
     torch.cuda.empty_cache()
+    if hasattr(torch._C, "_host_emptyCache"):
+        torch._C._host_emptyCache()
 
 
 @pytest.mark.parametrize("name", list(SMALL))
@@ -372,44 +376,64 @@ def test_timing_ring_keeps_back_to_back_steps():
 FULL = {"c2": C2, "c3": C3, "c4": C4, "c5": C5}
 
 
+def full_size_slots(w):
+    """Layer slots checked at full size: every slot of the 7B-32K workload,
+    slots 0, 1 and the last of the larger ones (whose host stores are 8 to
+    21 GiB per slot)."""
+    return list(range(w.n_slots)) if w.n_slots * w.k_bytes() <= (16 << 30) else \
+        [0, 1, w.n_slots - 1]
+
+
 @pytest.mark.parametrize("name", list(FULL))
-def test_full_size_layer_sampled_units(name):
-    """One layer at the workload's full per-layer size, through the layer loop
-    (the benchmark's launch configuration); sampled units against the oracle."""
+def test_full_size_layer_slots_sampled_units(name):
+    """Full per-layer size, several layer slots: each slot's standalone calls
+    against the oracle on sampled units (selection, attention, gathered bytes,
+    planted keys of every unit), then one decode step whose layers cycle all
+    those slots in the layer loop (the benchmark's launch configuration), bit
+    for bit equal to the standalone calls for every layer."""
     w = FULL[name]
-    s = Slot(w)
-    o = Outputs(w)
-    run_layer(w, s, o)
+    slot_ids = full_size_slots(w)
+    slots, ref = [], []
+    for sid in slot_ids:
+        s = Slot(w, sid)
+        o = Outputs(w)
+        run_layer(w, s, o)
+        torch.cuda.synchronize()
+        idx, sel, lse = o.idx.cpu().numpy(), o.sel.cpu().numpy(), o.lse.cpu().numpy()
+        out = o.out.cpu().numpy()
+        units = sample_units(w.units, n=5, seed=w.cfg_id * 100 + sid)
+        for u in units:
+            check_unit_topk(w, s, u, idx[u], sel[u], lse)
+            check_unit_attention(w, s, u, idx[u], out)
+        check_gather(w, s, idx, o.k_buf, o.v_buf, units)
+        # properties that hold for every unit: ascending, in range, planted keys kept
+        assert np.all(np.diff(idx, axis=1) > 0) and idx.min() >= 0
+        assert idx.max() < w.ctx_len - w.window
+        if w.n_planted:
+            P = w.n_planted
+            for u in range(w.units):
+                b, hk = divmod(u, w.n_kv_heads)
+                assert np.all(np.isin(s.planted[b, hk, :P], idx[u])), f"slot {sid} unit {u}"
+        slots.append(s)
+        ref.append(o.out.clone())
+        del o
+        _free()
+    # One decode step over len(slots) + 2 layers, layer l on slot l % len(slots).
+    L = len(slots) + 2
     ctx = dd.Ctx(dd_shape(w))
-    outs = [torch.empty_like(o.out) for _ in range(2)]
+    outs = [torch.full_like(ref[0], float("nan")) for _ in range(L)]
     compute = torch.cuda.Stream()
     copy = torch.cuda.Stream(priority=-1)
     compute.wait_stream(torch.cuda.current_stream())
-    ctx.decode_step(_layers(w, [s], outs, 2), compute=compute, copy=copy)
+    ctx.decode_step(_layers(w, slots, outs, L), compute=compute, copy=copy)
     torch.cuda.synchronize()
-    assert torch.equal(outs[0], o.out) and torch.equal(outs[1], o.out)
+    for l in range(L):
+        assert torch.equal(outs[l], ref[l % len(slots)]), f"layer {l} (slot {slot_ids[l % len(slots)]})"
     # the fused form of steps 1-2 (its last-CTA selection samples at these sizes too)
-    fused = [torch.full_like(o.out, float("nan"))]
-    ctx.decode_step(_layers(w, [s], fused, 1), compute=compute, copy=copy, fused_topk=True)
+    fused = [torch.full_like(ref[0], float("nan"))]
+    ctx.decode_step(_layers(w, slots[:1], fused, 1), compute=compute, copy=copy, fused_topk=True)
     torch.cuda.synchronize()
-    assert torch.equal(fused[0], o.out)
-    idx, sel, lse = o.idx.cpu().numpy(), o.sel.cpu().numpy(), o.lse.cpu().numpy()
-    out = o.out.cpu().numpy()
-    units = sample_units(w.units, n=5, seed=w.cfg_id)
-    for u in units:
-        check_unit_topk(w, s, u, idx[u], sel[u], lse)
-        check_unit_attention(w, s, u, idx[u], out)
-        if w.n_planted:
-            b, hk = divmod(u, w.n_kv_heads)
-            assert set(s.planted[b, hk, :w.n_planted].tolist()) <= set(idx[u].tolist())
-    check_gather(w, s, idx, o.k_buf, o.v_buf, units)
-    # properties that hold for every unit: ascending, in range, planted keys kept
-    assert np.all(np.diff(idx, axis=1) > 0) and idx.min() >= 0 and idx.max() < w.ctx_len - w.window
-    if w.n_planted:
-        P = w.n_planted
-        for u in range(w.units):
-            b, hk = divmod(u, w.n_kv_heads)
-            assert np.all(np.isin(s.planted[b, hk, :P], idx[u]))
+    assert torch.equal(fused[0], ref[0])
     ctx.close()
-    del s, o, outs
+    del slots, ref, outs, fused
     _free()

@@ -56,3 +56,29 @@ def test_noalloc_rejects_shapes_beyond_its_static_scratch():
     status = dd.lib().dd_sparse_decode_attn_noalloc(ctypes.byref(big.c()), 16, 16, 16, 16, None,
                                                     16, None)
     assert status == dd.DD_ERR_UNSUPPORTED
+
+
+@pytest.mark.gpu
+def test_noalloc_rejects_the_pointers_the_workspace_call_rejects():
+    """Both attention entry points share one pointer check: a page-locked host
+    buffer passed as the query (or as the output) is refused by each with
+    DD_ERR_INVALID_ARG before anything is launched."""
+    w = CASES[0]
+    s, o = Slot(w), Outputs(w)
+    run_layer(w, s, o)
+    torch.cuda.synchronize()
+    q_host = s.q.cpu().pin_memory()
+    out_host = torch.empty(o.out.shape, dtype=o.out.dtype).pin_memory()
+    shape = ctypes.byref(dd_shape(w).c())
+    stream = torch.cuda.current_stream().cuda_stream
+    v_win = s.v_win.data_ptr() if s.v_win is not None else None
+    for q_ptr, out_ptr in ((q_host.data_ptr(), o.out.data_ptr()),
+                           (s.q.data_ptr(), out_host.data_ptr())):
+        st_noalloc = dd.lib().dd_sparse_decode_attn_noalloc(
+            shape, q_ptr, o.k_buf.data_ptr(), o.v_buf.data_ptr(), s.K.data_ptr(), v_win, out_ptr,
+            stream)
+        st_ws = dd.lib().dd_sparse_decode_attn(
+            shape, q_ptr, o.k_buf.data_ptr(), o.v_buf.data_ptr(), s.K.data_ptr(), v_win, out_ptr,
+            o.ws.data_ptr(), o.ws.numel(), stream)
+        assert st_noalloc == dd.DD_ERR_INVALID_ARG
+        assert st_ws == dd.DD_ERR_INVALID_ARG
