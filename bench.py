@@ -65,7 +65,9 @@ def parse():
     p.add_argument("--repeats", type=int, default=5,
                    help="back-to-back timed regions of --steps steps; value is the median")
     p.add_argument("--profile-case", action="store_true",
-                   help="small case for ncu captures: batch 2, 2 layers, 1 slot")
+                   help="small case for ncu captures: batch --profile-batch, 2 layers, 1 slot")
+    p.add_argument("--profile-batch", type=int, default=2,
+                   help="batch of the --profile-case workload")
     p.add_argument("--gather-mode", type=int, default=None, choices=[0, 1],
                    help="0: bulk-copy gather, 1: load/store gather (default: 0, or 1 with "
                         "--landmarks, where whole chunks make it the faster one)")
@@ -111,7 +113,7 @@ def resolve_defaults(args):
 def workload(args):
     w = synth.WORKLOADS[args.workload]
     if args.profile_case:
-        w = w.scaled(batch=2, n_layers=2, n_slots=1)
+        w = w.scaled(batch=args.profile_batch, n_layers=2, n_slots=1)
     if args.slots:
         w = w.scaled(n_slots=args.slots)
     return w

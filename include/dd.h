@@ -162,6 +162,10 @@ dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes);
  *   idx_out  device [B][H_kv][k] int32     sel_score_out device [B][H_kv][k]
  *   lse_out  device [B][H_q] fp32 (may be NULL)
  *   workspace device, at least dd_workspace_size bytes.
+ * Passage: summary page, core formulas (alpha = softmax(q_spec K^T /
+ * sqrt(d_k)), I = argtopk(alpha, k)) and worked example, step 4; paper Sec. 1
+ * (the retrieval index comes from the token being processed and the key
+ * state); paper Fig. 1 "Select Top-k".
  */
 dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k_dev,
                         int32_t* idx_out, float* sel_score_out, float* lse_out, void* workspace,
@@ -185,7 +189,14 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
  *                       tiles back with bulk stores (used by dd_decode_step);
  *                   1 = load/store gather: 16-byte loads from every thread;
  *                   other values return DD_ERR_UNSUPPORTED.  Both modes give
- *                   identical bytes.
+ *                   identical bytes.  (Neither is a batched copy-engine
+ *                   copy: one copy-engine request per 256-byte row would be
+ *                   bound by its submission cost, and the one-call batched
+ *                   copy routines are not used by this library.)
+ * Passage: paper Sec. 2.2 (the host link is far slower than HBM and the
+ * selected entries are scattered over the context, so only they are fetched);
+ * paper Fig. 1 "Sparse KV Gather"; summary page worked example, step 5 (about
+ * 2 MB per layer and request for LLaMA-2-7B at 32K with the top 128).
  */
 dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v_host,
                         const int32_t* idx, void* k_buf, void* v_buf, int mode,
@@ -214,6 +225,10 @@ dd_status dd_set_gather_geometry(int grid_pct, int tile_bytes, int stages);
  *   q      device [B][H_q][d]        k_buf, v_buf device [B][H_kv][k][d]
  *   k_dev  device [B][H_kv][n][d]    v_win device [B][H_kv][W][d] (NULL if W=0)
  *   out    device [B][H_q][d] fp32
+ * Passage: paper Fig. 1 "Attention" (decode attention over the fetched sparse
+ * KV entries); paper Sec. 2.1 (attention of the current query over the cached
+ * keys and values); summary page worked example, step 7 (the prefetched
+ * entries serve the decoding step).
  */
 dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void* k_buf,
                                 const void* v_buf, const void* k_dev, const void* v_win,
@@ -352,12 +367,19 @@ typedef struct {
  * Allocate the layer-scoped state for one shape: two scratch slots of
  * gathered K/V rows (2 x 2 x B*H_kv*k*d elements; independent of n), two index
  * slots, the workspace and the events.  Returns DD_ERR_OOM on allocation
- * failure.  Uses the current CUDA device; the context is bound to it.
+ * failure.  Uses the current CUDA device; the context is bound to it.  The
+ * number of layers is not fixed here: each dd_decode_step passes its own
+ * layer list, and the per-layer state is what the two slots hold.
  */
 dd_status dd_ctx_create(const dd_shape* shape, dd_ctx** out);
 void dd_ctx_destroy(dd_ctx* ctx);
 
-/* Bytes of device memory a context holds (scratch slots + workspace). */
+/* Bytes of device memory a context holds: the two layer slots (gathered K
+ * and V rows, 2 x 2 x B*H_kv*k*d elements; their indices and selection
+ * scores, 2 x 2 x B*H_kv*k x 4 bytes), the query heads' LSE (B*H_q x 4 bytes)
+ * and the workspace (dd_workspace_size; its fp32 logits, 4 bytes per query
+ * head and position, are the only part that grows with n), plus the
+ * miss-correction and landmark buffers once those are used. */
 size_t dd_ctx_device_bytes(const dd_ctx* ctx);
 
 enum {
@@ -415,7 +437,17 @@ dd_status dd_ctx_set_landmark_chunk(dd_ctx* ctx, int chunk);
  * last read its slot, and each attention after its gather.  The copy stream
  * is joined back into `compute` before return.  If copy == compute (or copy
  * is NULL) every phase runs in order on `compute` (the serial schedule, with
- * bit-identical results).
+ * bit-identical results).  Flags that choose a schedule other than the
+ * pipeline (DD_STEP_LATE_GATHER, DD_STEP_GATHER_BESIDE_ATTN) together with
+ * DD_STEP_PIPELINE return DD_ERR_UNSUPPORTED; in the serial schedule every
+ * phase already runs alone, so they have no effect there.
+ * Per-phase times are read afterwards with dd_ctx_timings (flags
+ * DD_STEP_TIMING / DD_STEP_TIMING_LIGHT) instead of an output array, so that
+ * steps can be enqueued back to back without a host wait.
+ * Passage: paper Sec. 1 (layer-aware transfer schedule; layer-scoped KV memory
+ * manager); summary page, core formulas (T_transfer = sum_l S_l / B hidden by
+ * min max(T_compute, T_transfer); buffer O(n d) -> O(k d)) and worked example,
+ * step 6 (the transfer overlaps the attention of other layers).
  */
 dd_status dd_decode_step(dd_ctx* ctx, const dd_layer_io* layers, int n_layers,
                          dd_stream_t compute, dd_stream_t copy, int flags);

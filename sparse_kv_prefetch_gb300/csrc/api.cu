@@ -685,6 +685,9 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   const bool correct = (flags & DD_STEP_CORRECT_MISSES) != 0;
   const bool use_lm = (flags & DD_STEP_LANDMARKS) != 0;
   const bool fused = (flags & DD_STEP_FUSED_TOPK) != 0;
+  if ((flags & DD_STEP_PIPELINE) &&
+      (flags & (DD_STEP_LATE_GATHER | DD_STEP_GATHER_BESIDE_ATTN)))
+    return DD_ERR_UNSUPPORTED;  // schedules that exclude each other
   const bool delay_copy = (flags & DD_STEP_DEBUG_DELAY_COPY) != 0;
   const bool delay_compute = (flags & DD_STEP_DEBUG_DELAY_COMPUTE) != 0;
   constexpr uint64_t kDebugDelayNs = 50000;  // 50 us before each gather / attention

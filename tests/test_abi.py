@@ -74,6 +74,18 @@ def test_workspace_size_layout():
         assert ws % 256 == 0
 
 
+def test_gather_geometry_ranges():
+    """dd_set_gather_geometry takes grid 1..800 % of the SMs, tiles of a
+    multiple of 512 bytes up to 16 KiB, 1..8 stages, and at most 227 KiB of
+    shared memory per CTA; anything else is refused and changes nothing."""
+    lib = dd.lib()
+    for bad in ((0, 4096, 3), (801, 4096, 3), (100, 4000, 3), (100, 256, 3),
+                (100, 32768, 1), (100, 4096, 0), (100, 4096, 9), (100, 16384, 8)):
+        assert lib.dd_set_gather_geometry(*bad) == dd.DD_ERR_INVALID_ARG, bad
+    for good in ((1, 512, 1), (800, 16384, 6), (100, 4096, 3)):
+        assert lib.dd_set_gather_geometry(*good) == dd.DD_OK, good
+
+
 def test_null_and_misaligned_pointers_rejected():
     lib = dd.lib()
     shp = _shape().c()

@@ -72,7 +72,38 @@ def test_layer_small(name):
     torch.cuda.synchronize()
     assert torch.equal(kb1.view(torch.uint8), o.k_buf.view(torch.uint8))
     assert torch.equal(vb1.view(torch.uint8), o.v_buf.view(torch.uint8))
+    # so does the bulk-copy gather in every geometry: few or many CTAs, one
+    # stage or many, tiles narrower than a row or of many rows
+    try:
+        for geom in ((1, 512, 1), (13, 16384, 6), (400, 2048, 8), (100, 8192, 2)):
+            dd.set_gather_geometry(*geom)
+            kb1.zero_()
+            vb1.zero_()
+            dd.gather_h2d(dd_shape(w), s.K_h, s.V_h, o.idx, kb1, vb1, mode=0)
+            torch.cuda.synchronize()
+            assert torch.equal(kb1.view(torch.uint8), o.k_buf.view(torch.uint8)), geom
+            assert torch.equal(vb1.view(torch.uint8), o.v_buf.view(torch.uint8)), geom
+    finally:
+        dd.set_gather_geometry()
     dd.check_device()
+
+
+def test_exclusive_schedule_flags_rejected():
+    """The pipeline schedule cannot also be the late-gather or the guarded
+    overlap schedule: such a step is refused before anything is enqueued."""
+    w = SMALL["c2_mini"]
+    s = Slot(w)
+    ctx = dd.Ctx(dd_shape(w))
+    outs = [torch.empty((w.batch, w.n_q_heads, w.head_dim), device="cuda") for _ in range(2)]
+    layers = _layers(w, [s], outs, 2)
+    copy = torch.cuda.Stream()
+    for kw in (dict(pipeline=True, guarded=True), dict(pipeline=True, late_gather=True)):
+        with pytest.raises(dd.DDError) as e:
+            ctx.decode_step(layers, copy=copy, **kw)
+        assert e.value.status == dd.DD_ERR_UNSUPPORTED
+    ctx.decode_step(layers, copy=copy, guarded=True, late_gather=True)
+    torch.cuda.synchronize()
+    ctx.close()
 
 
 def test_host_store_from_dd_host_alloc():
