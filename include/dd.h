@@ -215,6 +215,14 @@ dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v
  * the ranges.  The bytes gathered never depend on it.
  */
 dd_status dd_set_gather_geometry(int grid_pct, int tile_bytes, int stages);
+/*
+ * Geometry of the load/store gather (mode 1) for every later launch in the
+ * process: grid_pct CTAs per 100 SMs (1..800) of `threads` threads (a multiple
+ * of 32, 32..256), each thread with 8 16-byte loads in flight.  The default is
+ * (100, 256).  DD_ERR_INVALID_ARG outside the ranges.  The bytes gathered
+ * never depend on it.
+ */
+dd_status dd_set_gather_lsu_geometry(int grid_pct, int threads);
 
 /*
  * Step 4 for one layer: out[b,h] = sum_{j in S} softmax_S(q[b,h] . K_j /

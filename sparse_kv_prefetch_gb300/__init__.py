@@ -118,6 +118,7 @@ def _lib():
             "dd_host_store_locked": ([ctypes.c_void_p], ctypes.c_int),
             "dd_workspace_size": ([S, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
             "dd_set_gather_geometry": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_int),
+            "dd_set_gather_lsu_geometry": ([ctypes.c_int, ctypes.c_int], ctypes.c_int),
             "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dd_gather_h2d": ([S, P, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
             "dd_sparse_decode_attn": ([S, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
@@ -247,6 +248,11 @@ def check_device():
 def set_gather_geometry(grid_pct: int = 100, tile_bytes: int = 4096, stages: int = 3):
     """Geometry of the bulk-copy gather for later launches (see dd.h)."""
     _check(_lib().dd_set_gather_geometry(grid_pct, tile_bytes, stages), "dd_set_gather_geometry")
+
+
+def set_gather_lsu_geometry(grid_pct: int = 100, threads: int = 256):
+    """Geometry of the load/store gather for later launches (see dd.h)."""
+    _check(_lib().dd_set_gather_lsu_geometry(grid_pct, threads), "dd_set_gather_lsu_geometry")
 
 
 def workspace_size(shape: Shape) -> int:

@@ -205,6 +205,10 @@ dd_status dd_set_gather_geometry(int grid_pct, int tile_bytes, int stages) {
   return set_gather_geometry(grid_pct, tile_bytes, stages);
 }
 
+dd_status dd_set_gather_lsu_geometry(int grid_pct, int threads) {
+  return set_gather_lsu_geometry(grid_pct, threads);
+}
+
 dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes) {
   if (!bytes) return DD_ERR_INVALID_ARG;
   Dims d;

@@ -57,6 +57,9 @@ cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
 // Geometry of the bulk-copy gather (mode 0), process-wide: grid in percent
 // of the SM count, bytes per tensor of a shared-memory stage, stages per CTA.
 dd_status set_gather_geometry(int grid_pct, int tile_bytes, int stages);
+// The same for the load/store gather (mode 1): grid in percent of the SM
+// count, threads per CTA (a multiple of 32, at most 256).
+dd_status set_gather_lsu_geometry(int grid_pct, int threads);
 // Host stores allocated by the library (hoststore.cu).
 // True if p lies in a store from dd_host_alloc (transparent huge pages,
 // registered with CUDA), whose translations the gather prefetches.

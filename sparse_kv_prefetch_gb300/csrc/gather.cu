@@ -24,7 +24,7 @@
 //
 // mode 1, gather_lsu_kernel: every thread keeps kInFlight 16-byte loads from
 //   host memory outstanding (consecutive threads read consecutive 16-byte
-//   pieces of a row).  Kept as the plain reference design.
+//   pieces of a row) through the load/store pipeline.
 #include <algorithm>
 #include <atomic>
 
@@ -196,30 +196,32 @@ cudaError_t launch_tma(const Dims& d, const void* kh, const void* vh, const int3
 }
 
 // ------------------------------------------------------------ mode 1 (LSU)
-#ifndef DD_GATHER_LSU_THREADS
-#define DD_GATHER_LSU_THREADS 256
-#endif
-constexpr int kLsuThreads = DD_GATHER_LSU_THREADS;
+// Geometry of a launch: `threads` per CTA (one to eight warps), grid in
+// percent of the SM count, kInFlight 16-byte loads outstanding per thread.
+// One warp per CTA needs about 2 K registers, which fit beside three GQA
+// scoring CTAs on an SM; dd_set_gather_lsu_geometry changes it process-wide.
+constexpr int kLsuMaxThreads = 256;
 constexpr int kInFlight = 8;
+std::atomic<int> g_lsu_grid_pct{100}, g_lsu_threads{256};
 
 template <int CPR>  // 16-byte pieces per row
-__global__ void __launch_bounds__(kLsuThreads)
+__global__ void __launch_bounds__(kLsuMaxThreads)
     gather_lsu_kernel(const uint4* __restrict__ k_host, const uint4* __restrict__ v_host,
                       const int32_t* __restrict__ idx, uint4* __restrict__ k_buf,
                       uint4* __restrict__ v_buf, int n, int k, long long rows) {
   // Piece p of the flattened work list: row r = p / (2 CPR), tensor t (K or
-  // V) = (p / CPR) & 1, part = p % CPR.
+  // V) = (p / CPR) & 1, part = p % CPR.  Consecutive threads read consecutive
+  // pieces of a row.  Host lines are read once: streaming loads.
   const long long total = rows * 2 * CPR;
-  const long long stride = (long long)gridDim.x * kLsuThreads;
-  for (long long p0 = (long long)blockIdx.x * kLsuThreads + threadIdx.x; p0 < total;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long p0 = (long long)blockIdx.x * blockDim.x + threadIdx.x; p0 < total;
        p0 += stride * kInFlight) {
     uint4 v[kInFlight];
-    long long dst[kInFlight];
-    int tv[kInFlight];
+    uint4* dst[kInFlight];
 #pragma unroll
     for (int i = 0; i < kInFlight; ++i) {
       const long long p = p0 + i * stride;
-      tv[i] = -1;
+      dst[i] = nullptr;
       if (p < total) {
         const unsigned r = (unsigned)(p / (2 * CPR));
         const int t = (int)((p / CPR) & 1);
@@ -227,16 +229,13 @@ __global__ void __launch_bounds__(kLsuThreads)
         const unsigned u = r / (unsigned)k;
         const int j = min(max(__ldg(idx + r), 0), n - 1);  // never read outside the store
         const uint4* src = (t ? v_host : k_host) + (((long long)u * n + j) * CPR + part);
-        v[i] = ld_ro(src);
-        dst[i] = (long long)r * CPR + part;
-        tv[i] = t;
+        v[i] = ld_stream(src);
+        dst[i] = (t ? v_buf : k_buf) + ((long long)r * CPR + part);
       }
     }
 #pragma unroll
-    for (int i = 0; i < kInFlight; ++i) {
-      if (tv[i] == 0) k_buf[dst[i]] = v[i];
-      if (tv[i] == 1) v_buf[dst[i]] = v[i];
-    }
+    for (int i = 0; i < kInFlight; ++i)
+      if (dst[i]) *dst[i] = v[i];
   }
 }
 
@@ -246,13 +245,14 @@ cudaError_t launch_lsu(const Dims& d, const void* kh, const void* vh, const int3
   static unsigned long long prepared = 0;
   cudaError_t e = prepare_kernel(gather_lsu_kernel<CPR>, &prepared, 0);
   if (e != cudaSuccess) return e;
+  const int threads = g_lsu_threads.load();
   const long long rows = (long long)d.U * d.k;
-  const long long work = (rows * 2 * CPR + (long long)kLsuThreads * kInFlight - 1) /
-                         ((long long)kLsuThreads * kInFlight);
-  long long grid = sm_count();  // one CTA per SM at most
+  const long long work = (rows * 2 * CPR + (long long)threads * kInFlight - 1) /
+                         ((long long)threads * kInFlight);
+  long long grid = ((long long)sm_count() * g_lsu_grid_pct.load() + 99) / 100;
   if (grid > work) grid = work;
   if (grid < 1) grid = 1;
-  gather_lsu_kernel<CPR><<<(unsigned)grid, kLsuThreads, 0, st>>>(
+  gather_lsu_kernel<CPR><<<(unsigned)grid, threads, 0, st>>>(
       static_cast<const uint4*>(kh), static_cast<const uint4*>(vh), idx,
       static_cast<uint4*>(kb), static_cast<uint4*>(vb), d.n, d.k, rows);
   return cudaGetLastError();
@@ -305,6 +305,15 @@ dd_status set_gather_geometry(int grid_pct, int tile_bytes, int stages) {
   g_grid_pct.store(grid_pct);
   g_tile_bytes.store(tile_bytes);
   g_stages.store(stages);
+  return DD_OK;
+}
+
+dd_status set_gather_lsu_geometry(int grid_pct, int threads) {
+  if (grid_pct < 1 || grid_pct > 800 || threads < 32 || threads > kLsuMaxThreads ||
+      threads % 32 != 0)
+    return DD_ERR_INVALID_ARG;
+  g_lsu_grid_pct.store(grid_pct);
+  g_lsu_threads.store(threads);
   return DD_OK;
 }
 
