@@ -22,7 +22,7 @@ baseline.
                   [--impl ours|reference] [--workload NAME]
                   [--schedule auto|overlap|late|pipeline|serial|guarded]
                   [--landmarks C] [--fused-topk] [--correct-misses]
-                  [--gather-mode 0|1] [--host-alloc huge|pinned] [--profile-case]
+                  [--gather-mode 0|1] [--host-alloc pinned|huge|torch] [--profile-case]
 
 The schedule defaults to auto: overlap, serial, pipeline or guarded, whichever a
 short calibration after the warm-up measures fastest on this host and workload.
@@ -48,11 +48,13 @@ import synth  # noqa: E402
 METRIC = "sparse-decode layer-steps/s; scoring HBM GB/s; gather host-link GB/s"
 UNIT = "layer-steps/s"
 FALLBACK_HBM_GBS = 6800.0
-# DRAM read + write bytes of one scoring launch, from the ncu captures in
-# profiles/ (batch 2: 64 units), scaled by units to the 7B-32K layer (256
-# units); traffic grows with the units processed.  Keyed by (workload, top-k
-# fused into the scoring kernel); absent where no capture of that kernel exists.
-SCORE_TRAFFIC_BYTES = {("c2-7b-32k", False): 545.35e6 * 256 / 64}
+# DRAM read + write bytes of one scoring launch, from ncu captures of the
+# current kernel (profiles/), scaled by units to the full layer.  GQA-128K: a
+# batch-16 capture (128 units: 4.2957 GB read, 0.2134 GB of logits written,
+# mean of two launches) doubled for the 256 units of the layer.  Keyed by
+# (workload, top-k fused into the scoring kernel); absent where no capture of
+# the current kernel exists.
+SCORE_TRAFFIC_BYTES = {("c5-gqa-128k", False): 2 * (4295654912 + 213407360)}
 
 
 def parse():
@@ -71,9 +73,14 @@ def parse():
     p.add_argument("--gather-mode", type=int, default=None, choices=[0, 1],
                    help="0: bulk-copy gather, 1: load/store gather (default: 0, or 1 with "
                         "--landmarks, where whole chunks make it the faster one)")
-    p.add_argument("--host-alloc", default="huge", choices=["huge", "pinned"],
-                   help="host KV store: dd_host_alloc (transparent huge pages, locked and "
-                        "registered) or torch pinned memory (64 KiB pages)")
+    p.add_argument("--host-alloc", default="pinned", choices=["pinned", "huge", "torch"],
+                   help="host KV store: dd_host_alloc_pinned (driver-allocated page-locked "
+                        "memory, exact size; stable), dd_host_alloc (locked transparent huge "
+                        "pages: faster gathers while the host leaves them alone, collapses "
+                        "when it splits and moves them), or torch pinned memory")
+    p.add_argument("--fill", default="auto", choices=["auto", "device", "cpu"],
+                   help="how the host store is written: device-to-host copies of the "
+                        "generated data (as a KV offload writes it), or CPU writes (auto)")
     p.add_argument("--copy-priority", default="high", choices=["high", "low"],
                    help="priority of the copy stream relative to the compute stream")
     p.add_argument("--slots", type=int, default=0,
@@ -288,6 +295,7 @@ def config_of(w, args):
             "parallelism": f"replicas x{args.gpus} (independent requests per GPU)",
             "gather_mode": ["bulk_copy", "load_store"][args.gather_mode],
             "host_store": args.host_alloc,
+            "host_store_fill": getattr(args, "fill_used", args.fill),
             "schedule": getattr(args, "schedule_chosen", args.schedule),
             "copy_stream_priority": args.copy_priority,
             "correct_misses": bool(args.correct_misses),
@@ -331,13 +339,13 @@ def run_ours(args, rank, world):
     D, L = w.n_slots, w.n_layers
 
     # Host store and the device-resident key cache, per layer slot.  The
-    # store defaults to dd_host_alloc's huge pages: with 64 KiB pages every
-    # long-context gather needs hundreds of thousands of page translations,
-    # which slows the gather and the scoring beside it.
+    # store defaults to driver-allocated page-locked memory, which the host
+    # never moves; huge pages gather faster while the host leaves them alone
+    # but were split and moved on many hosts (see dd.h).
     huge0 = anon_huge_bytes()
-    if args.host_alloc == "huge":
-        K_h = dd.host_empty((D, B, Hkv, n, d), dt)
-        V_h = dd.host_empty((D, B, Hkv, n, d), dt)
+    if args.host_alloc in ("huge", "pinned"):
+        K_h = dd.host_empty((D, B, Hkv, n, d), dt, kind=args.host_alloc)
+        V_h = dd.host_empty((D, B, Hkv, n, d), dt, kind=args.host_alloc)
     else:
         K_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
         V_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
@@ -346,12 +354,36 @@ def run_ours(args, rank, world):
     qs_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
     q_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
     t_gen = time.perf_counter()
-    for s in range(D):
-        synth.fill_slot(w, s, qs_h[s], q_h[s], K_h[s], V_h[s])
+    fill = args.fill if args.fill != "auto" else "cpu"
+    args.fill_used = fill
+    if fill == "device":
+        # As a KV offload writes it: each slot is generated on the CPU into
+        # page-locked staging, copied to the device (the key cache) and written
+        # into the host store by device-to-host copies.
+        K_d = torch.empty((D, B, Hkv, n, d), dtype=dt, device=dev)
+        K_st = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
+        V_st = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
+        v_tmp = torch.empty((B, Hkv, n, d), dtype=dt, device=dev)
+        vwin_d = torch.empty((D, B, Hkv, W, d), dtype=dt, device=dev) if W > 0 else None
+        for s in range(D):
+            synth.fill_slot(w, s, qs_h[s], q_h[s], K_st, V_st)
+            K_d[s].copy_(K_st)
+            K_h[s].copy_(K_d[s])
+            v_tmp.copy_(V_st)
+            V_h[s].copy_(v_tmp)
+            if W > 0:
+                vwin_d[s].copy_(v_tmp[:, :, n - W:, :])
+        torch.cuda.synchronize()
+        del K_st, V_st, v_tmp
+        if hasattr(torch._C, "_host_emptyCache"):
+            torch._C._host_emptyCache()
+    else:
+        for s in range(D):
+            synth.fill_slot(w, s, qs_h[s], q_h[s], K_h[s], V_h[s])
+        K_d = K_h.to(dev)
+        vwin_d = V_h[:, :, :, n - W:, :].contiguous().to(dev) if W > 0 else None
     t_gen = time.perf_counter() - t_gen
-    K_d = K_h.to(dev)
     qs_d, q_d = qs_h.to(dev), q_h.to(dev)
-    vwin_d = V_h[:, :, :, n - W:, :].contiguous().to(dev) if W > 0 else None
     outs = torch.empty((L, B, Hq, d), dtype=torch.float32, device=dev)
 
     shape = dd.Shape(B, Hq, Hkv, d, n, k, W, w.dtype)
@@ -418,7 +450,9 @@ def run_ours(args, rank, world):
     t_settle = time.perf_counter()
     settle_rounds, settle_gbs = 0, []
     good = 0
-    while True:
+    # (A round of a small workload is launch-bound, so its rate says nothing
+    # about the link: no wait then.)
+    while w.gather_bytes() * D >= (64 << 20):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(compute)
         for i in range(D):
@@ -434,7 +468,8 @@ def run_ours(args, rank, world):
         if good == 0:
             time.sleep(0.5)
     host_link = {"settle_s": time.perf_counter() - t_settle, "settle_rounds": settle_rounds,
-                 "settled": good >= 2, "last_round_gbs": settle_gbs[-4:]}
+                 "settled": good >= 2 if settle_rounds else None,
+                 "last_round_gbs": settle_gbs[-4:]}
 
     gather_alone = {}
     for mode in (0, 1):

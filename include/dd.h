@@ -123,16 +123,31 @@ dd_status dd_check_device(void);
  * CPU and releases it with dd_host_free.  Returns DD_ERR_OOM if the mapping
  * fails and DD_ERR_CUDA if registration fails.  Any page-locked memory works
  * with the gather.
- * Measured on GB300 (512 MiB huge pages, a 64 GiB store filled by the CPU and
- * cycled by gathers): locked, the gather held 183-188 GB/s; registered but not
- * locked, the host split some huge pages and migrated pages once the GPU
- * started reading, and gathers fell to 1-3 GB/s for the rest of the run.
+ * Measured on GB300 (512 MiB huge pages, a 64 GiB store filled and cycled by
+ * gathers): when the host leaves it alone the gather holds 183-188 GB/s.  On
+ * many freshly started hosts, though, the host split some of its huge pages
+ * and migrated pages soon after the store was filled (by CPU writes or by
+ * device-to-host copies alike, locked or not), and gathers then ran at
+ * 1-10 GB/s for minutes; dd_host_alloc_pinned is the stable alternative.
  */
 dd_status dd_host_alloc(size_t bytes, void** out);
-/* Unlock, unregister and unmap a region from dd_host_alloc (NULL is a
- * no-op); DD_ERR_INVALID_ARG for any other pointer. */
+/*
+ * Host KV store in page-locked memory that the CUDA driver allocates
+ * (cudaHostAlloc, portable), exactly `bytes`, in the host's base pages.  It
+ * is the stable choice: on GB300 hosts the huge-page store of dd_host_alloc
+ * gathers faster (183-188 against 131-176 GB/s on the GQA-128K layer) but
+ * was, in most runs on freshly started hosts, split and moved by the host
+ * shortly after it was filled, and its gathers then ran at 1-10 GB/s for
+ * minutes; stores from this call never did.  Contents start undefined.
+ * Released with dd_host_free.  DD_ERR_OOM if the allocation fails.
+ */
+dd_status dd_host_alloc_pinned(size_t bytes, void** out);
+/* Release a region from dd_host_alloc (unlock, unregister, unmap) or
+ * dd_host_alloc_pinned (NULL is a no-op); DD_ERR_INVALID_ARG for any other
+ * pointer. */
 dd_status dd_host_free(void* p);
-/* 1 if p lies in a store from dd_host_alloc, else 0. */
+/* 1 if p lies in a store from dd_host_alloc, 2 if from dd_host_alloc_pinned,
+ * else 0. */
 int dd_host_store_kind(const void* p);
 /* 1 if p lies in a store from dd_host_alloc whose pages are locked, else 0. */
 int dd_host_store_locked(const void* p);
@@ -187,7 +202,9 @@ dd_status dd_score_topk(const dd_shape* shape, const void* q_spec, const void* k
  *   mode            0 = bulk-copy gather: one-warp CTAs issue one
  *                       cp.async.bulk per row into shared memory and write
  *                       tiles back with bulk stores (used by dd_decode_step);
- *                   1 = load/store gather: 16-byte loads from every thread;
+ *                   1 = load/store gather: 16-byte loads from every thread
+ *                       (the gathered rows of one tensor, B*H_kv*k*d
+ *                       elements, below 8 GiB, else DD_ERR_UNSUPPORTED);
  *                   other values return DD_ERR_UNSUPPORTED.  Both modes give
  *                   identical bytes.  (Neither is a batched copy-engine
  *                   copy: one copy-engine request per 256-byte row would be
@@ -218,9 +235,12 @@ dd_status dd_set_gather_geometry(int grid_pct, int tile_bytes, int stages);
 /*
  * Geometry of the load/store gather (mode 1) for every later launch in the
  * process: grid_pct CTAs per 100 SMs (1..800) of `threads` threads (a multiple
- * of 32, 32..256), each thread with 8 16-byte loads in flight.  The default is
- * (100, 256).  DD_ERR_INVALID_ARG outside the ranges.  The bytes gathered
- * never depend on it.
+ * of 32 up to 256; 32 means one warp with 16 16-byte loads in flight per
+ * thread, more threads 8 loads each), or threads = 0 (the default, with
+ * grid_pct 100): chosen per shape to fit beside the scoring kernel that runs
+ * at the same time, one 16-deep warp per SM for groups of 4 or more query
+ * heads, eight warps per SM otherwise.  DD_ERR_INVALID_ARG outside the
+ * ranges.  The bytes gathered never depend on it.
  */
 dd_status dd_set_gather_lsu_geometry(int grid_pct, int threads);
 

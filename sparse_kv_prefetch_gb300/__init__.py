@@ -115,6 +115,8 @@ def _lib():
             "dd_host_free": ([ctypes.c_void_p], ctypes.c_int),
             "dd_host_page_bytes": ([], ctypes.c_size_t),
             "dd_host_store_kind": ([ctypes.c_void_p], ctypes.c_int),
+            "dd_host_alloc_pinned": ([ctypes.c_size_t, ctypes.POINTER(ctypes.c_void_p)],
+                                     ctypes.c_int),
             "dd_host_store_locked": ([ctypes.c_void_p], ctypes.c_int),
             "dd_workspace_size": ([S, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
             "dd_set_gather_geometry": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_int),
@@ -206,9 +208,10 @@ def version() -> int:
     return _lib().dd_version()
 
 
-def host_empty(shape, dtype):
-    """An uninitialised CPU tensor in a locked, page-locked huge-page host
-    region from dd_host_alloc (the recommended host KV store); freed with
+def host_empty(shape, dtype, kind: str = "huge"):
+    """An uninitialised CPU tensor in a page-locked host KV store from the
+    library: kind "huge" (dd_host_alloc: locked transparent huge pages) or
+    "pinned" (dd_host_alloc_pinned: driver-allocated, exact size).  Freed with
     dd_host_free when the tensor and all its views are gone."""
     import weakref
 
@@ -218,7 +221,12 @@ def host_empty(shape, dtype):
         numel *= int(s_)
     nbytes = max(1, numel * torch.empty((), dtype=dtype).element_size())
     p = ctypes.c_void_p()
-    _check(_lib().dd_host_alloc(nbytes, ctypes.byref(p)), "dd_host_alloc")
+    if kind == "huge":
+        _check(_lib().dd_host_alloc(nbytes, ctypes.byref(p)), "dd_host_alloc")
+    elif kind == "pinned":
+        _check(_lib().dd_host_alloc_pinned(nbytes, ctypes.byref(p)), "dd_host_alloc_pinned")
+    else:
+        raise ValueError(f"unknown host store kind {kind!r}")
     buf = (ctypes.c_char * nbytes).from_address(p.value)
     weakref.finalize(buf, _lib().dd_host_free, ctypes.c_void_p(p.value))
     t = torch.frombuffer(buf, dtype=torch.uint8, count=nbytes)
@@ -250,7 +258,7 @@ def set_gather_geometry(grid_pct: int = 100, tile_bytes: int = 4096, stages: int
     _check(_lib().dd_set_gather_geometry(grid_pct, tile_bytes, stages), "dd_set_gather_geometry")
 
 
-def set_gather_lsu_geometry(grid_pct: int = 100, threads: int = 256):
+def set_gather_lsu_geometry(grid_pct: int = 100, threads: int = 0):
     """Geometry of the load/store gather for later launches (see dd.h)."""
     _check(_lib().dd_set_gather_lsu_geometry(grid_pct, threads), "dd_set_gather_lsu_geometry")
 

@@ -154,6 +154,10 @@ bool is_device_ptr(const void* p) {
   return a.type == cudaMemoryTypeDevice && cudaGetDevice(&dev) == cudaSuccess && a.device == dev;
 }
 
+bool lsu_gather_fits(const Dims& d) {
+  return (long long)d.U * d.k * d.d * d.elt < (8ll << 30);  // 16-byte piece index range
+}
+
 bool all_device(std::initializer_list<const void*> ps) {
   for (const void* p : ps)
     if (p && !is_device_ptr(p)) return false;
@@ -244,6 +248,7 @@ dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v
   dd_status st = resolve(shape, &d);
   if (st != DD_OK) return st;
   if (mode != 0 && mode != 1) return DD_ERR_UNSUPPORTED;
+  if (mode == 1 && !lsu_gather_fits(d)) return DD_ERR_UNSUPPORTED;
   if (!k_host || !v_host || !idx || !k_buf || !v_buf) return DD_ERR_INVALID_ARG;
   if (!aligned16(k_host) || !aligned16(v_host) || !aligned16(k_buf) || !aligned16(v_buf))
     return DD_ERR_INVALID_ARG;
@@ -686,6 +691,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   const bool timing = light || (flags & DD_STEP_TIMING) != 0;
   const bool phases = timing && !light;  // the events of every phase
   const int gather_mode = (flags & DD_STEP_GATHER_LSU) ? 1 : 0;
+  if (gather_mode == 1 && !lsu_gather_fits(d)) return DD_ERR_UNSUPPORTED;
   const bool correct = (flags & DD_STEP_CORRECT_MISSES) != 0;
   const bool use_lm = (flags & DD_STEP_LANDMARKS) != 0;
   const bool fused = (flags & DD_STEP_FUSED_TOPK) != 0;

@@ -71,6 +71,9 @@ const void* host_to_device(const void* p);
 // Pointer checks of the C ABI (api.cu): device memory of the current device,
 // or managed memory; all_device accepts NULL entries.
 bool is_device_ptr(const void* p);
+// The load/store gather (mode 1) indexes 16-byte pieces with 31 bits: the
+// gathered rows of one tensor must stay below 8 GiB.
+bool lsu_gather_fits(const Dims& d);
 bool all_device(std::initializer_list<const void*> ps);
 // Where the attention reads the window's keys: row off + i (i < W) of each
 // unit's `stride` rows starting at p.

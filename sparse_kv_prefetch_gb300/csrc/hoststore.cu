@@ -10,6 +10,12 @@
 // touches hundreds of thousands of them.  dd_host_alloc gives the store
 // transparent huge pages instead: anonymous memory, faulted in from the CPU,
 // locked (mlock) and registered with CUDA (cudaHostRegister).
+// dd_host_alloc_pinned is the alternative that stays put: page-locked memory
+// the CUDA driver allocates itself (cudaHostAlloc), in the host's base pages.
+// On the GB300 hosts measured, huge-page stores had pages split and moved by
+// the host now and then, whatever the locking, and every read of the store
+// from the GPU slowed to a few GB/s while that lasted; driver-allocated
+// memory never did.
 //
 // Any page-locked host memory known to CUDA (torch pin_memory,
 // cudaHostAlloc) works with the gather as well.
@@ -49,9 +55,12 @@ size_t host_page_bytes() {
 
 namespace {
 
+enum Kind { kHuge = 1, kPinned = 2 };
+
 struct Region {
-  size_t len;   // bytes the caller may use (whole huge pages)
-  bool locked;  // mlock succeeded
+  size_t len;   // bytes the caller may use
+  int kind;
+  bool locked;  // kHuge: mlock succeeded
 };
 
 std::mutex g_mu;
@@ -71,7 +80,8 @@ const Region* find_region(const void* p, uintptr_t* base) {
 
 bool in_huge_page_store(const void* p) {
   std::lock_guard<std::mutex> lock(g_mu);
-  return find_region(p, nullptr) != nullptr;
+  const Region* r = find_region(p, nullptr);
+  return r && r->kind == kHuge;
 }
 
 const void* host_to_device(const void* p) {
@@ -139,7 +149,23 @@ dd_status dd_host_alloc(size_t bytes, void** out) {
   }
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    g_regions[(uintptr_t)p] = Region{len, locked};
+    g_regions[(uintptr_t)p] = Region{len, kHuge, locked};
+  }
+  *out = p;
+  return DD_OK;
+}
+
+dd_status dd_host_alloc_pinned(size_t bytes, void** out) {
+  if (!out || bytes == 0) return DD_ERR_INVALID_ARG;
+  *out = nullptr;
+  void* p = nullptr;
+  if (cudaHostAlloc(&p, bytes, cudaHostAllocPortable) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return DD_ERR_OOM;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    g_regions[(uintptr_t)p] = Region{bytes, kPinned, false};
   }
   *out = p;
   return DD_OK;
@@ -155,6 +181,7 @@ dd_status dd_host_free(void* p) {
     r = it->second;
     g_regions.erase(it);
   }
+  if (r.kind == kPinned) return cudaFreeHost(p) == cudaSuccess ? DD_OK : DD_ERR_CUDA;
   const cudaError_t e = cudaHostUnregister(p);
   if (r.locked) munlock(p, r.len);
   munmap(p, r.len);
@@ -165,7 +192,8 @@ size_t dd_host_page_bytes(void) { return host_page_bytes(); }
 
 int dd_host_store_kind(const void* p) {
   std::lock_guard<std::mutex> lock(g_mu);
-  return find_region(p, nullptr) ? 1 : 0;
+  const Region* r = find_region(p, nullptr);
+  return r ? r->kind : 0;
 }
 
 int dd_host_store_locked(const void* p) {

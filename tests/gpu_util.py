@@ -33,16 +33,18 @@ def orc_shape(w) -> oracle.Shape:
 class Slot:
     """One layer slot: pinned host store (q_spec, q, K, V) and device copies."""
 
-    def __init__(self, w, slot: int = 0, device: str = "cuda", fill=True, huge_pages=False):
+    def __init__(self, w, slot: int = 0, device: str = "cuda", fill=True, huge_pages=False,
+                 store: str = "torch"):
         dt = torch_dtype(w)
         B, Hq, Hkv, d, n, W = (w.batch, w.n_q_heads, w.n_kv_heads, w.head_dim, w.ctx_len,
                                w.window)
         self.w = w
         self.q_spec_h = torch.empty((B, Hq, d), dtype=dt, pin_memory=True)
         self.q_h = torch.empty((B, Hq, d), dtype=dt, pin_memory=True)
-        if huge_pages:  # the library's host store allocator
-            self.K_h = dd.host_empty((B, Hkv, n, d), dt)
-            self.V_h = dd.host_empty((B, Hkv, n, d), dt)
+        if huge_pages or store in ("huge", "pinned"):  # the library's host store allocators
+            kind = "huge" if huge_pages else store
+            self.K_h = dd.host_empty((B, Hkv, n, d), dt, kind=kind)
+            self.V_h = dd.host_empty((B, Hkv, n, d), dt, kind=kind)
         else:  # plain page-locked memory from torch
             self.K_h = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
             self.V_h = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)

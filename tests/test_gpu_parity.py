@@ -83,8 +83,18 @@ def test_layer_small(name):
             torch.cuda.synchronize()
             assert torch.equal(kb1.view(torch.uint8), o.k_buf.view(torch.uint8)), geom
             assert torch.equal(vb1.view(torch.uint8), o.v_buf.view(torch.uint8)), geom
+        # and the load/store gather: one deep warp, eight warps, the automatic choice
+        for lsu in ((100, 32), (30, 256), (100, 0)):
+            dd.set_gather_lsu_geometry(*lsu)
+            kb1.zero_()
+            vb1.zero_()
+            dd.gather_h2d(dd_shape(w), s.K_h, s.V_h, o.idx, kb1, vb1, mode=1)
+            torch.cuda.synchronize()
+            assert torch.equal(kb1.view(torch.uint8), o.k_buf.view(torch.uint8)), lsu
+            assert torch.equal(vb1.view(torch.uint8), o.v_buf.view(torch.uint8)), lsu
     finally:
         dd.set_gather_geometry()
+        dd.set_gather_lsu_geometry()
     dd.check_device()
 
 
@@ -103,6 +113,29 @@ def test_exclusive_schedule_flags_rejected():
         assert e.value.status == dd.DD_ERR_UNSUPPORTED
     ctx.decode_step(layers, copy=copy, guarded=True, late_gather=True)
     torch.cuda.synchronize()
+    ctx.close()
+
+
+def test_host_store_from_dd_host_alloc_pinned():
+    """The gather and the layer loop on a driver-allocated store from
+    dd_host_alloc_pinned (no huge-page touch kernel)."""
+    w = SMALL["c5_mini"]
+    s = Slot(w, store="pinned")
+    assert dd.lib().dd_host_store_kind(s.K_h.data_ptr()) == 2
+    o = Outputs(w)
+    run_layer(w, s, o)
+    torch.cuda.synchronize()
+    idx = o.idx.cpu().numpy()
+    check_gather(w, s, idx, o.k_buf, o.v_buf, range(w.units))
+    out = o.out.cpu().numpy()
+    for u in range(w.units):
+        check_unit_attention(w, s, u, idx[u], out)
+    ctx = dd.Ctx(dd_shape(w))
+    step_out = [torch.empty_like(o.out) for _ in range(2)]
+    ctx.decode_step(_layers(w, [s], step_out, 2), timing=True)
+    torch.cuda.synchronize()
+    assert torch.equal(step_out[0], o.out) and torch.equal(step_out[1], o.out)
+    assert ctx.timings()["launches"] == 4 * 2  # score, top-k, gather, attention per layer
     ctx.close()
 
 
