@@ -71,8 +71,9 @@ def parse():
     p.add_argument("--profile-batch", type=int, default=2,
                    help="batch of the --profile-case workload")
     p.add_argument("--gather-mode", type=int, default=None, choices=[0, 1],
-                   help="0: bulk-copy gather, 1: load/store gather (default: 0, or 1 with "
-                        "--landmarks, where whole chunks make it the faster one)")
+                   help="0: bulk-copy gather, 1: load/store gather (default: chosen with the "
+                        "schedule by the calibration; 0, or 1 with --landmarks, when the "
+                        "schedule is given)")
     p.add_argument("--host-alloc", default="pinned", choices=["pinned", "huge", "torch"],
                    help="host KV store: dd_host_alloc_pinned (driver-allocated page-locked "
                         "memory, exact size; stable), dd_host_alloc (locked transparent huge "
@@ -108,12 +109,31 @@ def parse():
                    help="1: start each layer's gather after the previous attention")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="CPU work budget of the oracle baseline")
-    p.add_argument("--settle-seconds", type=float, default=90.0,
+    p.add_argument("--settle-seconds", type=float, default=60.0,
                    help="longest wait for the host link to reach steady state before measuring")
     return p.parse_args()
 
 
+# Gather variants the calibration tries: (tag, mode, geometry).  The small
+# bulk-copy geometry fits beside the scoring kernel; the wide one keeps 5x the
+# rows in flight, which pays on stores of small pages (translation latency);
+# the load/store gather sizes itself to the scoring kernel beside it.
+GATHER_VARIANTS = (("bulk_copy_small", 0, (100, 4096, 3)),
+                   ("bulk_copy_wide", 0, (200, 8192, 4)),
+                   ("load_store", 1, (100, 0)))
+
+
+def set_gather_variant(dd, mode, geom):
+    if mode == 0:
+        dd.set_gather_geometry(*geom)
+    else:
+        dd.set_gather_lsu_geometry(*geom)
+
+
 def resolve_defaults(args):
+    # The gather kernel is part of the automatic choice when the schedule is:
+    # calibration then tries both (bulk copy and load/store).
+    args.gather_auto = args.gather_mode is None and args.schedule == "auto"
     if args.gather_mode is None:
         args.gather_mode = 1 if args.landmarks else 0
     return args
@@ -294,6 +314,7 @@ def config_of(w, args):
                   % (w.k_bytes() / 2**20),
             "parallelism": f"replicas x{args.gpus} (independent requests per GPU)",
             "gather_mode": ["bulk_copy", "load_store"][args.gather_mode],
+            "gather_variant": getattr(args, "gather_chosen", None),
             "host_store": args.host_alloc,
             "host_store_fill": getattr(args, "fill_used", args.fill),
             "schedule": getattr(args, "schedule_chosen", args.schedule),
@@ -442,34 +463,37 @@ def run_ours(args, rank, world):
             dd.score_topk(shape, qs_d[s_], K_d[s_], g_idx[s_], g_sel, g_lse, g_ws,
                           stream=compute)
     # Host-link steady state.  On this kind of host, periods of host-side
-    # memory management (page compaction and migration in the process) slow
-    # every GPU read of host memory ten-fold or more for seconds to minutes.
-    # Before measuring, gathers of one layer run alone (cycling the slots)
-    # until two rounds in a row reach 60 % of the copy probe, for at most
-    # --settle-seconds; how long that took is reported.
+    # memory management (huge pages split, pages migrated) slow every GPU read
+    # of host memory ten-fold or more for seconds to minutes.  Before
+    # measuring, rounds of single-layer gathers (one per layer slot) run back
+    # to back until the median gather of two rounds in a row reaches 60 % of
+    # the copy probe, for at most --settle-seconds; how long that took is
+    # reported.  (No pauses between rounds: after an idle spell the first
+    # gathers over a store of small pages run with cold translations.)
     t_settle = time.perf_counter()
     settle_rounds, settle_gbs = 0, []
     good = 0
     # (A round of a small workload is launch-bound, so its rate says nothing
     # about the link: no wait then.)
     while w.gather_bytes() * D >= (64 << 20):
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(compute)
+        evs = []
         for i in range(D):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(compute)
             dd.gather_h2d(shape, K_h[i % D], V_h[i % D], g_idx[i % D], g_kb, g_vb, stream=compute)
-        e1.record(compute)
-        e1.synchronize()
-        gbs = w.gather_bytes() * D / (e0.elapsed_time(e1) * 1e-3) / 1e9
+            e1.record(compute)
+            evs.append((e0, e1))
+        torch.cuda.synchronize()
+        gbs = w.gather_bytes() / (statistics.median(a_.elapsed_time(b_) for a_, b_ in evs)
+                                  * 1e-3) / 1e9
         settle_rounds += 1
         settle_gbs.append(round(gbs, 1))
         good = good + 1 if gbs >= 0.6 * probe_gbs else 0
         if good >= 2 or time.perf_counter() - t_settle > args.settle_seconds:
             break
-        if good == 0:
-            time.sleep(0.5)
     host_link = {"settle_s": time.perf_counter() - t_settle, "settle_rounds": settle_rounds,
                  "settled": good >= 2 if settle_rounds else None,
-                 "last_round_gbs": settle_gbs[-4:]}
+                 "last_round_median_gbs": settle_gbs[-4:]}
 
     gather_alone = {}
     for mode in (0, 1):
@@ -579,12 +603,18 @@ def run_ours(args, rank, world):
     if args.schedule == "auto":
         # Calibration: each two-stream schedule and the serial one in turn,
         # 3 steps each, twice.
-        cands = (("overlap", copy, False, False), ("serial", None, False, False),
-                 ("pipeline", copy, True, False), ("guarded", copy, False, True))
-        cal = {name: 0.0 for name, _, _, _ in cands}
+        base = (("overlap", copy, False, False), ("serial", None, False, False),
+                ("pipeline", copy, True, False), ("guarded", copy, False, True))
+        variants = GATHER_VARIANTS if args.gather_auto else \
+            tuple(v for v in GATHER_VARIANTS if v[1] == args.gather_mode)[:1]
+        cands = tuple((name + "+" + vt, cs, pp, gg, vm, vg) for vt, vm, vg in variants
+                      for name, cs, pp, gg in base)
+        cal = {c[0]: 0.0 for c in cands}
         for _ in range(2):
-            for name, cs, pp, gg in cands:
+            for name, cs, pp, gg, gm, geom in cands:
                 pipe, guard = pp, gg  # read by step()
+                args.gather_mode = gm
+                set_gather_variant(dd, gm, geom)
                 c0 = torch.cuda.Event(enable_timing=True)
                 c1 = torch.cuda.Event(enable_timing=True)
                 c0.record(compute)
@@ -593,14 +623,16 @@ def run_ours(args, rank, world):
                 c1.record(compute)
                 torch.cuda.synchronize()
                 cal[name] += c0.elapsed_time(c1) / 6
-        names = [name for name, _, _, _ in cands]
+        names = [c[0] for c in cands]
         pick = min(cal, key=cal.get)
         if world > 1:  # every rank runs the same schedule: rank 0's choice
             import torch.distributed as dist
             t = torch.tensor([names.index(pick)], device=dev)
             dist.broadcast(t, 0)
             pick = names[int(t)]
-        _, sched_copy, pipe, guard = cands[names.index(pick)]
+        _, sched_copy, pipe, guard, args.gather_mode, geom = cands[names.index(pick)]
+        set_gather_variant(dd, args.gather_mode, geom)
+        args.gather_chosen = pick.split("+", 1)[1]
         args.schedule_chosen = (f"{pick} (auto; calibration ms per step: "
                                 + ", ".join(f"{k} {v:.2f}" for k, v in cal.items()) + ")")
     n_phase = max(3, args.steps // 2)
