@@ -22,10 +22,13 @@ baseline.
                   [--impl ours|reference] [--workload NAME]
                   [--schedule auto|overlap|late|pipeline|serial|guarded]
                   [--landmarks C] [--fused-topk] [--correct-misses]
-                  [--gather-mode 0|1] [--host-alloc auto|pinned|huge|torch] [--profile-case]
+                  [--gather-mode 0|1] [--host-alloc pinned|huge|auto|torch] [--profile-case]
 
-The schedule defaults to auto: overlap, serial, pipeline or guarded, whichever a
-short calibration after the warm-up measures fastest on this host and workload.
+The host store defaults to driver-allocated page-locked memory.  The schedule
+and the gather variant default to auto: overlap, serial, pipeline or guarded,
+each with the small or wide bulk-copy gather or the load/store one, whichever
+a short calibration after the warm-up measures fastest on this host and
+workload.
 """
 from __future__ import annotations
 
@@ -74,13 +77,14 @@ def parse():
                    help="0: bulk-copy gather, 1: load/store gather (default: chosen with the "
                         "schedule by the calibration; 0, or 1 with --landmarks, when the "
                         "schedule is given)")
-    p.add_argument("--host-alloc", default="auto", choices=["auto", "pinned", "huge", "torch"],
-                   help="host KV store: dd_host_alloc (locked transparent huge pages: faster "
-                        "gathers while the host leaves them alone, collapses when it splits "
-                        "and moves them), dd_host_alloc_pinned (driver-allocated page-locked "
-                        "memory, exact size; stable), torch pinned memory, or auto: the "
-                        "huge-page store if its gathers reach steady state within "
-                        "--settle-seconds, else the driver-allocated one")
+    p.add_argument("--host-alloc", default="pinned", choices=["pinned", "huge", "auto", "torch"],
+                   help="host KV store: dd_host_alloc_pinned (driver-allocated page-locked "
+                        "memory, exact size; stable: the default), dd_host_alloc (locked "
+                        "transparent huge pages: faster gathers while the host leaves them "
+                        "alone, collapses when it splits and moves them), auto (the huge-page "
+                        "store if its gathers reach steady state within --settle-seconds, else "
+                        "the driver-allocated one; it can still collapse later), or torch "
+                        "pinned memory")
     p.add_argument("--fill", default="auto", choices=["auto", "device", "cpu"],
                    help="how the host store is written: device-to-host copies of the "
                         "generated data (as a KV offload writes it), or CPU writes (auto)")
@@ -363,8 +367,9 @@ def run_ours(args, rank, world):
 
     # Host store and the device-resident key cache, per layer slot.  The
     # store defaults to driver-allocated page-locked memory, which the host
-    # never moves; huge pages gather faster while the host leaves them alone
-    # but were split and moved on many hosts (see dd.h).
+    # never moved in any run; huge pages gather faster while the host leaves
+    # them alone, but on many hosts it split and moved them, even minutes
+    # into a run (see dd.h).
     huge0 = anon_huge_bytes()
     store_kind = "huge" if args.host_alloc == "auto" else args.host_alloc
     if store_kind in ("huge", "pinned"):
@@ -470,9 +475,9 @@ def run_ours(args, rank, world):
     # of a huge-page store ten-fold or more, for seconds to minutes.  Before
     # measuring, rounds of single-layer gathers (one per layer slot) run back
     # to back until two rounds in a row agree within 10 % and reach a floor:
-    # 60 % of the copy probe for a huge-page store (a healthy one gathers at
-    # 0.85 of it), 25 % otherwise (stores of small pages are translation-bound
-    # well below the probe).  No pauses between rounds: after an idle spell the
+    # 45 % of the copy probe for a huge-page store (a healthy one gathers at
+    # 0.5-0.9 of it, a collapsed one at 0.005-0.05), 25 % otherwise (stores of
+    # small pages are translation-bound well below the probe).  No pauses between rounds: after an idle spell the
     # first gathers over small pages run with cold translations.
     def settle(kh, vh, floor, max_s):
         t0 = time.perf_counter()
@@ -500,7 +505,7 @@ def run_ours(args, rank, world):
         return {"settle_s": time.perf_counter() - t0, "settle_rounds": rounds,
                 "settled": good >= 1 if rounds else None, "last_round_median_gbs": rates[-4:]}
 
-    host_link = settle(K_h, V_h, 0.6 if store_kind == "huge" else 0.25, args.settle_seconds)
+    host_link = settle(K_h, V_h, 0.45 if store_kind == "huge" else 0.25, args.settle_seconds)
     store_note = store_kind
     if args.host_alloc == "auto" and host_link["settled"] is False:
         # The huge-page store did not reach steady state: free it and write
