@@ -123,10 +123,10 @@ def parse():
 # Gather variants the calibration tries: (tag, mode, geometry).  The small
 # bulk-copy geometry fits beside the scoring kernel; the wide one keeps 5x the
 # rows in flight, which pays on stores of small pages (translation latency);
-# the load/store gather sizes itself to the scoring kernel beside it.
+# the load/store gather (eight warps per SM) takes no shared memory.
 GATHER_VARIANTS = (("bulk_copy_small", 0, (100, 4096, 3)),
                    ("bulk_copy_wide", 0, (200, 8192, 4)),
-                   ("load_store", 1, (100, 0)))
+                   ("load_store", 1, (100, 256)))
 
 
 def set_gather_variant(dd, mode, geom):

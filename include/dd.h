@@ -235,12 +235,9 @@ dd_status dd_set_gather_geometry(int grid_pct, int tile_bytes, int stages);
 /*
  * Geometry of the load/store gather (mode 1) for every later launch in the
  * process: grid_pct CTAs per 100 SMs (1..800) of `threads` threads (a multiple
- * of 32 up to 256; 32 means one warp with 16 16-byte loads in flight per
- * thread, more threads 8 loads each), or threads = 0 (the default, with
- * grid_pct 100): chosen per shape to fit beside the scoring kernel that runs
- * at the same time, one 16-deep warp per SM for groups of 4 or more query
- * heads, eight warps per SM otherwise.  DD_ERR_INVALID_ARG outside the
- * ranges.  The bytes gathered never depend on it.
+ * of 32, 32..256), each thread with 8 16-byte loads in flight.  The default is
+ * (100, 256).  DD_ERR_INVALID_ARG outside the ranges.  The bytes gathered
+ * never depend on it.
  */
 dd_status dd_set_gather_lsu_geometry(int grid_pct, int threads);
 

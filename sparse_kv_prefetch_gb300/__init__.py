@@ -258,7 +258,7 @@ def set_gather_geometry(grid_pct: int = 100, tile_bytes: int = 4096, stages: int
     _check(_lib().dd_set_gather_geometry(grid_pct, tile_bytes, stages), "dd_set_gather_geometry")
 
 
-def set_gather_lsu_geometry(grid_pct: int = 100, threads: int = 0):
+def set_gather_lsu_geometry(grid_pct: int = 100, threads: int = 256):
     """Geometry of the load/store gather for later launches (see dd.h)."""
     _check(_lib().dd_set_gather_lsu_geometry(grid_pct, threads), "dd_set_gather_lsu_geometry")
 

@@ -196,17 +196,14 @@ cudaError_t launch_tma(const Dims& d, const void* kh, const void* vh, const int3
 }
 
 // ------------------------------------------------------------ mode 1 (LSU)
-// Geometry of a launch: `threads` per CTA (one to eight warps), grid in
-// percent of the SM count, INFL 16-byte loads outstanding per thread.  By
-// default (threads = 0) the geometry is chosen to fit beside the scoring
-// kernel of the next layer, which runs at the same time on the other stream:
-// eight warps with 8 loads each in flight when the scoring kernel is the MHA
-// one (40 registers a thread: room for 16 K more registers on an SM), one
-// warp with 16 loads in flight, capped at 104 registers, beside the
-// grouped-query one (72 registers: three of its CTAs leave 3,328 registers).
-// dd_set_gather_lsu_geometry overrides it process-wide.
+// Geometry of a launch: `threads` per CTA (one to eight warps) and the grid
+// in percent of the SM count, each thread with kInFlight 16-byte loads in
+// flight; dd_set_gather_lsu_geometry changes it process-wide.  (One warp per
+// SM with 16 loads in flight, small enough to sit beside the grouped-query
+// scoring kernel, reached only 32-51 GB/s: too shallow for the host link.)
 constexpr int kLsuMaxThreads = 256;
-std::atomic<int> g_lsu_grid_pct{100}, g_lsu_threads{0};
+constexpr int kInFlight = 8;
+std::atomic<int> g_lsu_grid_pct{100}, g_lsu_threads{kLsuMaxThreads};
 
 template <int CPR, int INFL>  // 16-byte pieces per row, loads in flight per thread
 __device__ __forceinline__ void gather_lsu_body(const uint4* __restrict__ k_host,
@@ -252,46 +249,26 @@ __global__ void __launch_bounds__(kLsuMaxThreads)
     gather_lsu_kernel(const uint4* __restrict__ k_host, const uint4* __restrict__ v_host,
                       const int32_t* __restrict__ idx, uint4* __restrict__ k_buf,
                       uint4* __restrict__ v_buf, int n, int k, long long rows) {
-  gather_lsu_body<CPR, 8>(k_host, v_host, idx, k_buf, v_buf, n, k, rows);
-}
-
-// One warp, 16 loads in flight per thread, at most 104 registers a thread.
-template <int CPR>
-__global__ void __launch_bounds__(32, 19)
-    gather_lsu_warp_kernel(const uint4* __restrict__ k_host, const uint4* __restrict__ v_host,
-                           const int32_t* __restrict__ idx, uint4* __restrict__ k_buf,
-                           uint4* __restrict__ v_buf, int n, int k, long long rows) {
-  gather_lsu_body<CPR, 16>(k_host, v_host, idx, k_buf, v_buf, n, k, rows);
+  gather_lsu_body<CPR, kInFlight>(k_host, v_host, idx, k_buf, v_buf, n, k, rows);
 }
 
 template <int CPR>
 cudaError_t launch_lsu(const Dims& d, const void* kh, const void* vh, const int32_t* idx,
                        void* kb, void* vb, cudaStream_t st) {
-  static unsigned long long prepared = 0, prepared_warp = 0;
+  static unsigned long long prepared = 0;
   const long long rows = (long long)d.U * d.k;
   if (rows * 2 * CPR * 2 >= (1ll << 31)) return cudaErrorInvalidValue;  // piece index range
-  int threads = g_lsu_threads.load();
-  if (threads == 0) threads = d.G >= 4 ? 32 : kLsuMaxThreads;
-  const bool warp = threads == 32;
-  cudaError_t e = warp ? prepare_kernel(gather_lsu_warp_kernel<CPR>, &prepared_warp, 0)
-                       : prepare_kernel(gather_lsu_kernel<CPR>, &prepared, 0);
+  cudaError_t e = prepare_kernel(gather_lsu_kernel<CPR>, &prepared, 0);
   if (e != cudaSuccess) return e;
-  const int infl = warp ? 16 : 8;
-  const long long work = (rows * 2 * CPR + (long long)threads * infl - 1) /
-                         ((long long)threads * infl);
+  const int threads = g_lsu_threads.load();
+  const long long work = (rows * 2 * CPR + (long long)threads * kInFlight - 1) /
+                         ((long long)threads * kInFlight);
   long long grid = ((long long)sm_count() * g_lsu_grid_pct.load() + 99) / 100;
   if (grid > work) grid = work;
   if (grid < 1) grid = 1;
-  const uint4* k4 = static_cast<const uint4*>(kh);
-  const uint4* v4 = static_cast<const uint4*>(vh);
-  uint4* kb4 = static_cast<uint4*>(kb);
-  uint4* vb4 = static_cast<uint4*>(vb);
-  if (warp)
-    gather_lsu_warp_kernel<CPR><<<(unsigned)grid, 32, 0, st>>>(k4, v4, idx, kb4, vb4, d.n, d.k,
-                                                              rows);
-  else
-    gather_lsu_kernel<CPR><<<(unsigned)grid, threads, 0, st>>>(k4, v4, idx, kb4, vb4, d.n, d.k,
-                                                              rows);
+  gather_lsu_kernel<CPR><<<(unsigned)grid, threads, 0, st>>>(
+      static_cast<const uint4*>(kh), static_cast<const uint4*>(vh), idx,
+      static_cast<uint4*>(kb), static_cast<uint4*>(vb), d.n, d.k, rows);
   return cudaGetLastError();
 }
 
@@ -346,7 +323,7 @@ dd_status set_gather_geometry(int grid_pct, int tile_bytes, int stages) {
 }
 
 dd_status set_gather_lsu_geometry(int grid_pct, int threads) {
-  if (grid_pct < 1 || grid_pct > 800 || threads < 0 || threads > kLsuMaxThreads ||
+  if (grid_pct < 1 || grid_pct > 800 || threads < 32 || threads > kLsuMaxThreads ||
       threads % 32 != 0)
     return DD_ERR_INVALID_ARG;
   g_lsu_grid_pct.store(grid_pct);

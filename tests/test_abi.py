@@ -84,9 +84,9 @@ def test_gather_geometry_ranges():
         assert lib.dd_set_gather_geometry(*bad) == dd.DD_ERR_INVALID_ARG, bad
     for good in ((1, 512, 1), (800, 16384, 6), (100, 4096, 3)):
         assert lib.dd_set_gather_geometry(*good) == dd.DD_OK, good
-    for bad in ((0, 0), (100, 48), (100, 288), (100, -32)):
+    for bad in ((0, 256), (100, 48), (100, 288), (100, 0), (801, 32)):
         assert lib.dd_set_gather_lsu_geometry(*bad) == dd.DD_ERR_INVALID_ARG, bad
-    for good in ((100, 32), (50, 256), (100, 0)):
+    for good in ((100, 32), (50, 128), (100, 256)):
         assert lib.dd_set_gather_lsu_geometry(*good) == dd.DD_OK, good
 
 

@@ -83,8 +83,8 @@ def test_layer_small(name):
             torch.cuda.synchronize()
             assert torch.equal(kb1.view(torch.uint8), o.k_buf.view(torch.uint8)), geom
             assert torch.equal(vb1.view(torch.uint8), o.v_buf.view(torch.uint8)), geom
-        # and the load/store gather: one deep warp, eight warps, the automatic choice
-        for lsu in ((100, 32), (30, 256), (100, 0)):
+        # and the load/store gather: one warp per CTA, eight on a small grid, the default
+        for lsu in ((100, 32), (30, 256), (100, 256)):
             dd.set_gather_lsu_geometry(*lsu)
             kb1.zero_()
             vb1.zero_()
