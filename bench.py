@@ -85,6 +85,10 @@ def parse():
                         "store if its gathers reach steady state within --settle-seconds, else "
                         "the driver-allocated one; it can still collapse later), or torch "
                         "pinned memory")
+    p.add_argument("--host-layout", default="separate", choices=["interleaved", "separate"],
+                   help="host store layout: one store with each position's K row followed by "
+                        "its V row (a position's two rows share a page: fewer translations), "
+                        "or separate K and V stores")
     p.add_argument("--fill", default="auto", choices=["auto", "device", "cpu"],
                    help="how the host store is written: device-to-host copies of the "
                         "generated data (as a KV offload writes it), or CPU writes (auto)")
@@ -355,6 +359,102 @@ def run_reference(args, rank, world):
 
 # ---------------------------------------------------------------- our arm
 
+class HostStore:
+    """The layer slots' host KV store: separate K and V stores [D][B][H_kv][n][d]
+    or one interleaved store [D][B][H_kv][n][2][d] (each position's K row then
+    its V row), in driver-allocated page-locked memory, locked huge pages or
+    torch pinned memory."""
+
+    def __init__(self, dd, kind, layout, shape5, dt):
+        self.dd, self.kind, self.inter = dd, kind, layout == "interleaved"
+        D, B, Hkv, n, d = shape5
+
+        def alloc(shp):
+            if kind in ("huge", "pinned"):
+                return dd.host_empty(shp, dt, kind=kind)
+            return torch.empty(shp, dtype=dt, pin_memory=True)
+        if self.inter:
+            self.kv = alloc((D, B, Hkv, n, 2, d))
+            self.K, self.V = self.kv[:, :, :, :, 0, :], self.kv[:, :, :, :, 1, :]
+        else:
+            self.kv = None
+            self.K, self.V = alloc(shape5), alloc(shape5)
+        self.bytes = 2 * self.K.numel() * self.K.element_size()
+
+    def flat(self, s):
+        """Slot s as one contiguous host tensor (the copy-engine probe's source)."""
+        return (self.kv[s] if self.inter else self.K[s]).reshape(-1)
+
+    def fill(self, w, qs_h, q_h, dev, device_fill):
+        """Write every slot with the seeded generator.  Returns the device key
+        cache and the device window V."""
+        dd = self.dd
+        D, B, Hkv, n, d = self.K.shape
+        W = w.window
+        dt = self.K.dtype
+        K_d = torch.empty((D, B, Hkv, n, d), dtype=dt, device=dev)
+        vwin_d = torch.empty((D, B, Hkv, W, d), dtype=dt, device=dev) if W > 0 else None
+        if not device_fill and not self.inter:
+            for s in range(D):
+                synth.fill_slot(w, s, qs_h[s], q_h[s], self.K[s], self.V[s])
+                K_d[s].copy_(self.K[s])
+                if W > 0:
+                    vwin_d[s].copy_(self.V[s, :, :, n - W:, :])
+            return K_d, vwin_d
+        # Through page-locked staging: the interleaved store is written by
+        # strided copies, and a device fill (as a KV offload writes the store)
+        # by device-to-host copies.
+        K_st = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
+        V_st = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
+        v_tmp = torch.empty((B, Hkv, n, d), dtype=dt, device=dev) if device_fill else None
+        for s in range(D):
+            synth.fill_slot(w, s, qs_h[s], q_h[s], K_st, V_st)
+            K_d[s].copy_(K_st)
+            if device_fill:
+                v_tmp.copy_(V_st)
+                self.K[s].copy_(K_d[s])
+                self.V[s].copy_(v_tmp)
+            else:
+                self.K[s].copy_(K_st)
+                self.V[s].copy_(V_st)
+            if W > 0:
+                vwin_d[s].copy_(V_st[:, :, n - W:, :])
+        torch.cuda.synchronize()
+        del K_st, V_st, v_tmp
+        if hasattr(torch._C, "_host_emptyCache"):
+            torch._C._host_emptyCache()
+        return K_d, vwin_d
+
+    def slot_host(self, s):
+        """Slot s's K and V as contiguous host tensors (the oracle's inputs)."""
+        return self.K[s].contiguous(), self.V[s].contiguous()
+
+    def gather(self, shape, s, idx, kb, vb, mode=0, stream=None):
+        if self.inter:
+            self.dd.gather_h2d_kv(shape, self.kv[s], idx, kb, vb, mode=mode, stream=stream)
+        else:
+            self.dd.gather_h2d(shape, self.K[s], self.V[s], idx, kb, vb, mode=mode, stream=stream)
+
+    def correct(self, shape, s, q, k_dev, idx_spec, kb_spec, vb_spec, idx_true, kb, vb, miss,
+                mass, ws, stream=None):
+        if self.inter:
+            self.dd.correct_misses_kv(shape, q, k_dev, idx_spec, kb_spec, vb_spec, self.kv[s],
+                                      idx_true, kb, vb, miss, mass, ws, stream=stream)
+        else:
+            self.dd.correct_misses(shape, q, k_dev, idx_spec, kb_spec, vb_spec, self.K[s],
+                                   self.V[s], idx_true, kb, vb, miss, mass, ws, stream=stream)
+
+    def io(self, s):
+        """The host-store fields of a layer's LayerIO."""
+        if self.inter:
+            return dict(k_host=None, v_host=None, kv_host=self.kv[s])
+        return dict(k_host=self.K[s], v_host=self.V[s], kv_host=None)
+
+    def locked(self):
+        return self.dd.host_store_locked(self.kv if self.inter else self.K) \
+            if self.kind == "huge" else None
+
+
 def run_ours(args, rank, world):
     import sparse_kv_prefetch_gb300 as dd
 
@@ -372,45 +472,15 @@ def run_ours(args, rank, world):
     # into a run (see dd.h).
     huge0 = anon_huge_bytes()
     store_kind = "huge" if args.host_alloc == "auto" else args.host_alloc
-    if store_kind in ("huge", "pinned"):
-        K_h = dd.host_empty((D, B, Hkv, n, d), dt, kind=store_kind)
-        V_h = dd.host_empty((D, B, Hkv, n, d), dt, kind=store_kind)
-    else:
-        K_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
-        V_h = torch.empty((D, B, Hkv, n, d), dtype=dt, pin_memory=True)
-    store_bytes = 2 * K_h.numel() * K_h.element_size()
+    store = HostStore(dd, store_kind, args.host_layout, (D, B, Hkv, n, d), dt)
+    store_bytes = store.bytes
     huge_frac = (anon_huge_bytes() - huge0) / store_bytes if huge0 is not None else None
     qs_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
     q_h = torch.empty((D, B, Hq, d), dtype=dt, pin_memory=True)
     t_gen = time.perf_counter()
     fill = args.fill if args.fill != "auto" else "cpu"
     args.fill_used = fill
-    if fill == "device":
-        # As a KV offload writes it: each slot is generated on the CPU into
-        # page-locked staging, copied to the device (the key cache) and written
-        # into the host store by device-to-host copies.
-        K_d = torch.empty((D, B, Hkv, n, d), dtype=dt, device=dev)
-        K_st = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
-        V_st = torch.empty((B, Hkv, n, d), dtype=dt, pin_memory=True)
-        v_tmp = torch.empty((B, Hkv, n, d), dtype=dt, device=dev)
-        vwin_d = torch.empty((D, B, Hkv, W, d), dtype=dt, device=dev) if W > 0 else None
-        for s in range(D):
-            synth.fill_slot(w, s, qs_h[s], q_h[s], K_st, V_st)
-            K_d[s].copy_(K_st)
-            K_h[s].copy_(K_d[s])
-            v_tmp.copy_(V_st)
-            V_h[s].copy_(v_tmp)
-            if W > 0:
-                vwin_d[s].copy_(v_tmp[:, :, n - W:, :])
-        torch.cuda.synchronize()
-        del K_st, V_st, v_tmp
-        if hasattr(torch._C, "_host_emptyCache"):
-            torch._C._host_emptyCache()
-    else:
-        for s in range(D):
-            synth.fill_slot(w, s, qs_h[s], q_h[s], K_h[s], V_h[s])
-        K_d = K_h.to(dev)
-        vwin_d = V_h[:, :, :, n - W:, :].contiguous().to(dev) if W > 0 else None
+    K_d, vwin_d = store.fill(w, qs_h, q_h, dev, fill == "device")
     t_gen = time.perf_counter() - t_gen
     qs_d, q_d = qs_h.to(dev), q_h.to(dev)
     outs = torch.empty((L, B, Hq, d), dtype=torch.float32, device=dev)
@@ -436,8 +506,10 @@ def run_ours(args, rank, world):
     torch.cuda.synchronize()
 
     # Host-link probe: one large contiguous pinned H2D copy, median of 10.
-    probe_bytes = min(1 << 30, K_h[0].numel() * K_h.element_size())
-    src = K_h[0].view(-1).view(torch.uint8)[:probe_bytes]
+    flat0 = store.flat(0)
+    probe_bytes = min(1 << 30, flat0.numel() * flat0.element_size())
+    src = flat0.view(torch.uint8)[:probe_bytes]
+    del flat0
     dst = torch.empty(probe_bytes, dtype=torch.uint8, device=dev)
     probe = []
     for i in range(13):
@@ -479,7 +551,7 @@ def run_ours(args, rank, world):
     # 0.5-0.9 of it, a collapsed one at 0.005-0.05), 25 % otherwise (stores of
     # small pages are translation-bound well below the probe).  No pauses between rounds: after an idle spell the
     # first gathers over small pages run with cold translations.
-    def settle(kh, vh, floor, max_s):
+    def settle(floor, max_s):
         t0 = time.perf_counter()
         rounds, rates, good = 0, [], 0
         # (A round of a small workload is launch-bound: its rate says nothing.)
@@ -489,8 +561,7 @@ def run_ours(args, rank, world):
                 e0 = torch.cuda.Event(enable_timing=True)
                 e1 = torch.cuda.Event(enable_timing=True)
                 e0.record(compute)
-                dd.gather_h2d(shape, kh[i % D], vh[i % D], g_idx[i % D], g_kb, g_vb,
-                              stream=compute)
+                store.gather(shape, i % D, g_idx[i % D], g_kb, g_vb, stream=compute)
                 e1.record(compute)
                 evs.append((e0, e1))
             torch.cuda.synchronize()
@@ -505,36 +576,32 @@ def run_ours(args, rank, world):
         return {"settle_s": time.perf_counter() - t0, "settle_rounds": rounds,
                 "settled": good >= 1 if rounds else None, "last_round_median_gbs": rates[-4:]}
 
-    host_link = settle(K_h, V_h, 0.45 if store_kind == "huge" else 0.25, args.settle_seconds)
+    host_link = settle(0.45 if store_kind == "huge" else 0.25, args.settle_seconds)
     store_note = store_kind
     if args.host_alloc == "auto" and host_link["settled"] is False:
         # The huge-page store did not reach steady state: free it and write
         # the same (seeded) data into driver-allocated page-locked memory.
         import gc
-        del K_h, V_h
+        del store
         gc.collect()
-        K_h = dd.host_empty((D, B, Hkv, n, d), dt, kind="pinned")
-        V_h = dd.host_empty((D, B, Hkv, n, d), dt, kind="pinned")
+        store = HostStore(dd, "pinned", args.host_layout, (D, B, Hkv, n, d), dt)
         t_refill = time.perf_counter()
-        for s_ in range(D):
-            synth.fill_slot(w, s_, qs_h[s_], q_h[s_], K_h[s_], V_h[s_])
+        store.fill(w, qs_h, q_h, dev, fill == "device")
         t_gen += time.perf_counter() - t_refill
         store_kind = "pinned"
         store_note = ("pinned (the huge-page store did not settle within %.0f s; last rounds %s "
                       "GB/s)" % (host_link["settle_s"], host_link["last_round_median_gbs"]))
-        host_link = settle(K_h, V_h, 0.25, args.settle_seconds)
+        host_link = settle(0.25, args.settle_seconds)
     args.store_used = store_note
 
     gather_alone = {}
     for mode in (0, 1):
         for i in range(2 * D):
-            dd.gather_h2d(shape, K_h[i % D], V_h[i % D], g_idx[i % D], g_kb, g_vb, mode=mode,
-                          stream=compute)
+            store.gather(shape, i % D, g_idx[i % D], g_kb, g_vb, mode=mode, stream=compute)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(compute)
         for i in range(4 * D):
-            dd.gather_h2d(shape, K_h[i % D], V_h[i % D], g_idx[i % D], g_kb, g_vb, mode=mode,
-                          stream=compute)
+            store.gather(shape, i % D, g_idx[i % D], g_kb, g_vb, mode=mode, stream=compute)
         e1.record(compute)
         e1.synchronize()
         gather_alone[mode] = w.gather_bytes() * 4 * D / (e0.elapsed_time(e1) * 1e-3) / 1e9
@@ -548,9 +615,9 @@ def run_ours(args, rank, world):
         c_miss = torch.empty(U, dtype=torch.int32, device=dev)
         c_mass = torch.empty((U, 2), dtype=torch.float32, device=dev)
         for s_ in range(D):
-            dd.gather_h2d(shape, K_h[s_], V_h[s_], g_idx[s_], g_kb, g_vb, stream=compute)
-            dd.correct_misses(shape, q_d[s_], K_d[s_], g_idx[s_], g_kb, g_vb, K_h[s_], V_h[s_],
-                              c_idx, c_kb, c_vb, c_miss, c_mass, g_ws, stream=compute)
+            store.gather(shape, s_, g_idx[s_], g_kb, g_vb, stream=compute)
+            store.correct(shape, s_, q_d[s_], K_d[s_], g_idx[s_], g_kb, g_vb, c_idx, c_kb, c_vb,
+                          c_miss, c_mass, g_ws, stream=compute)
             compute.synchronize()
             pred_miss.append(c_miss.cpu().numpy().copy())
             pred_mass.append(c_mass.cpu().numpy().copy())
@@ -564,9 +631,9 @@ def run_ours(args, rank, world):
             for s_ in range(min(D, 2)):
                 q_sig = (qs_d[s_].float() + sigma * torch.randn(
                     qs_d[s_].shape, generator=gen, device=dev)).to(dt)
-                dd.gather_h2d(shape, K_h[s_], V_h[s_], g_idx[s_], g_kb, g_vb, stream=compute)
-                dd.correct_misses(shape, q_sig, K_d[s_], g_idx[s_], g_kb, g_vb, K_h[s_], V_h[s_],
-                                  c_idx, c_kb, c_vb, c_miss, c_mass, g_ws, stream=compute)
+                store.gather(shape, s_, g_idx[s_], g_kb, g_vb, stream=compute)
+                store.correct(shape, s_, q_sig, K_d[s_], g_idx[s_], g_kb, g_vb, c_idx, c_kb,
+                              c_vb, c_miss, c_mass, g_ws, stream=compute)
                 compute.synchronize()
                 miss.append(c_miss.cpu().numpy().copy())
             pred_sigma[str(sigma)] = float(1.0 - np.mean(miss) / k)
@@ -603,12 +670,13 @@ def run_ours(args, rank, world):
             vwin_d.numel() * vwin_d.element_size() if W else 0)
 
     def layer_io(l, qs, q):
+        h = store.io(l % D)
         if C:
-            return dd.LayerIO(qs, q, None, K_h[l % D], V_h[l % D],
+            return dd.LayerIO(qs, q, None, h["k_host"], h["v_host"],
                               vwin_d[l % D] if W > 0 else None, outs[l], lm_d[l % D],
-                              kwin_d[l % D] if W > 0 else None)
-        return dd.LayerIO(qs, q, K_d[l % D], K_h[l % D], V_h[l % D],
-                          vwin_d[l % D] if W > 0 else None, outs[l])
+                              kwin_d[l % D] if W > 0 else None, h["kv_host"])
+        return dd.LayerIO(qs, q, K_d[l % D], h["k_host"], h["v_host"],
+                          vwin_d[l % D] if W > 0 else None, outs[l], kv_host=h["kv_host"])
 
     layers = dd.Ctx.pack([layer_io(l, qs_d[l % D], q_d[l % D]) for l in range(L)])
 
@@ -790,7 +858,8 @@ def run_ours(args, rank, world):
 
     cpu = None
     if rank == 0 and world == 1 and not args.profile_case:
-        host = {"q_spec": qs_h[0], "q": q_h[0], "K": K_h[0], "V": V_h[0]}
+        K0_h, V0_h = store.slot_host(0)
+        host = {"q_spec": qs_h[0], "q": q_h[0], "K": K0_h, "V": V0_h}
         rate, cores, nl = oracle_layer_rate(w, host, args.cpu_seconds)
         cpu = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": f"{nl} whole layers of layer slot 0 (all {w.units} (request, KV head) "
@@ -866,7 +935,8 @@ def run_ours(args, rank, world):
         "host_store": {"bytes": store_bytes, "huge_page_bytes": dd.host_page_bytes(),
                        "huge_page_fraction": huge_frac,
                        "kind": store_kind,
-                       "locked": dd.host_store_locked(K_h) if store_kind == "huge" else None},
+                       "locked": store.locked(),
+                       "layout": args.host_layout},
         "host_link": host_link,
         "ctx_device_bytes": ctx.device_bytes,
         "hbm_resident_kv_bytes": resident,

@@ -220,6 +220,18 @@ dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v
                         dd_stream_t stream);
 
 /*
+ * Step 3 from one interleaved host store: kv_host is pinned host memory laid
+ * out [B][H_kv][n][2][d], each position's K row followed by its V row.
+ * Otherwise as dd_gather_h2d, with identical bytes gathered.  A position's
+ * two rows share a host page, so a gather over small pages needs fewer page
+ * translations than over separate K and V stores: 12 % fewer for the GQA-128K
+ * layer, 38 % fewer for the 7B-32K one with 64 KiB pages.
+ * Passage: as dd_gather_h2d; the interleaved layout is this design's.
+ */
+dd_status dd_gather_h2d_kv(const dd_shape* shape, const void* kv_host, const int32_t* idx,
+                           void* k_buf, void* v_buf, int mode, dd_stream_t stream);
+
+/*
  * Geometry of the bulk-copy gather (mode 0) for every later launch in the
  * process, by dd_gather_h2d and dd_decode_step alike: grid_pct one-warp CTAs
  * per 100 SMs (1..800), tile_bytes of rows per tensor and shared-memory stage
@@ -317,6 +329,14 @@ dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_
                             int32_t* idx_true_out, void* k_buf_out, void* v_buf_out,
                             int32_t* miss_out, float* mass_out, void* workspace, size_t ws_bytes,
                             dd_stream_t stream);
+/* dd_correct_misses with the rows the prediction missed read from one
+ * interleaved host store [B][H_kv][n][2][d] (see dd_gather_h2d_kv). */
+dd_status dd_correct_misses_kv(const dd_shape* shape, const void* q, const void* k_dev,
+                               const int32_t* idx_spec, const void* k_buf_spec,
+                               const void* v_buf_spec, const void* kv_host,
+                               int32_t* idx_true_out, void* k_buf_out, void* v_buf_out,
+                               int32_t* miss_out, float* mass_out, void* workspace,
+                               size_t ws_bytes, dd_stream_t stream);
 
 /*
  * Test hook (no counterpart in the paper): enqueue on `stream` a wait that
@@ -386,6 +406,10 @@ typedef struct {
                          they are read from k_dev.  Under DD_STEP_LANDMARKS with
                          k_win (or W = 0) k_dev may be NULL: nothing of size n
                          then stays on the device */
+  const void* kv_host; /* pinned host [B][H_kv][n][2][d]: one store holding each
+                          position's K row followed by its V row, in place of
+                          k_host and v_host (which must then be NULL); NULL to
+                          use k_host and v_host.  See dd_gather_h2d_kv */
 } dd_layer_io;
 
 /*

@@ -69,7 +69,8 @@ class dd_layer_io(ctypes.Structure):
     _fields_ = [("q_spec", ctypes.c_void_p), ("q", ctypes.c_void_p), ("k_dev", ctypes.c_void_p),
                 ("k_host", ctypes.c_void_p), ("v_host", ctypes.c_void_p),
                 ("v_win", ctypes.c_void_p), ("out", ctypes.c_void_p),
-                ("landmarks", ctypes.c_void_p), ("k_win", ctypes.c_void_p)]
+                ("landmarks", ctypes.c_void_p), ("k_win", ctypes.c_void_p),
+                ("kv_host", ctypes.c_void_p)]
 
 
 class dd_phase_times(ctypes.Structure):
@@ -123,6 +124,7 @@ def _lib():
             "dd_set_gather_lsu_geometry": ([ctypes.c_int, ctypes.c_int], ctypes.c_int),
             "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dd_gather_h2d": ([S, P, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
+            "dd_gather_h2d_kv": ([S, P, P, P, P, ctypes.c_int, P], ctypes.c_int),
             "dd_sparse_decode_attn": ([S, P, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
             "dd_sparse_decode_attn_noalloc": ([S, P, P, P, P, P, P, P], ctypes.c_int),
             "dd_ctx_create": ([S, ctypes.POINTER(P)], ctypes.c_int),
@@ -135,6 +137,8 @@ def _lib():
                                    ctypes.c_int),
             "dd_correct_misses": ([S, P, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
                                   ctypes.c_int),
+            "dd_correct_misses_kv": ([S, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P],
+                                     ctypes.c_int),
             "dd_ctx_correction_stats": ([P, P, P, ctypes.c_int], ctypes.c_int),
             "dd_landmarks_size": ([S, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t)],
                                   ctypes.c_int),
@@ -286,6 +290,13 @@ def gather_h2d(shape: Shape, k_host, v_host, idx, k_buf, v_buf, mode: int = 0, s
            "dd_gather_h2d")
 
 
+def gather_h2d_kv(shape: Shape, kv_host, idx, k_buf, v_buf, mode: int = 0, stream=None):
+    """Step 3 from one interleaved host store [B][H_kv][n][2][d]; see dd.h."""
+    _check(_lib().dd_gather_h2d_kv(ctypes.byref(shape.c()), _host(kv_host), _dev(idx),
+                                   _dev(k_buf), _dev(v_buf), mode, _stream(stream)),
+           "dd_gather_h2d_kv")
+
+
 def sparse_decode_attn(shape: Shape, q, k_buf, v_buf, k_dev, v_win, out, workspace, stream=None,
                        ws_bytes: Optional[int] = None):
     """Step 4: split-k attention over the gathered rows plus the window; see dd.h."""
@@ -309,6 +320,20 @@ def correct_misses(shape: Shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, k_h
         _dev(v_buf_spec), _host(k_host), _host(v_host), _dev(idx_true_out), _dev(k_buf_out),
         _dev(v_buf_out), _dev(miss_out), _dev(mass_out), _dev(workspace), ws_bytes,
         _stream(stream)), "dd_correct_misses")
+
+
+def correct_misses_kv(shape: Shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, kv_host,
+                      idx_true_out, k_buf_out, v_buf_out, miss_out, mass_out, workspace,
+                      stream=None, ws_bytes: Optional[int] = None):
+    """correct_misses with the host rows read from one interleaved store
+    [B][H_kv][n][2][d]; see dd.h."""
+    if ws_bytes is None:
+        ws_bytes = workspace.numel() * workspace.element_size()
+    _check(_lib().dd_correct_misses_kv(
+        ctypes.byref(shape.c()), _dev(q), _dev(k_dev), _dev(idx_spec), _dev(k_buf_spec),
+        _dev(v_buf_spec), _host(kv_host), _dev(idx_true_out), _dev(k_buf_out),
+        _dev(v_buf_out), _dev(miss_out), _dev(mass_out), _dev(workspace), ws_bytes,
+        _stream(stream)), "dd_correct_misses_kv")
 
 
 def landmarks_size(shape: Shape, chunk: int) -> int:
@@ -366,6 +391,7 @@ class LayerIO(NamedTuple):
     out: object
     landmarks: object = None
     k_win: object = None
+    kv_host: object = None
 
 
 class Ctx:
@@ -400,7 +426,7 @@ class Ctx:
         for i, io in enumerate(layers):
             arr[i] = dd_layer_io(_dev(io.q_spec), _dev(io.q), _dev(io.k_dev), _host(io.k_host),
                                  _host(io.v_host), _dev(io.v_win), _dev(io.out),
-                                 _dev(io.landmarks), _dev(io.k_win))
+                                 _dev(io.landmarks), _dev(io.k_win), _host(io.kv_host))
         return arr
 
     def set_landmark_chunk(self, chunk: int):

@@ -257,8 +257,28 @@ dd_status dd_gather_h2d(const dd_shape* shape, const void* k_host, const void* v
   if (!kh || !vh) return DD_ERR_INVALID_ARG;
   if (!all_device({idx, k_buf, v_buf})) return DD_ERR_INVALID_ARG;
   const bool touch = in_huge_page_store(k_host) || in_huge_page_store(v_host);
-  return cuda_status(launch_gather(d, kh, vh, idx, k_buf, v_buf, mode,
+  const HostKV h{kh, vh, (size_t)d.d * d.elt};
+  return cuda_status(launch_gather(d, h, idx, k_buf, v_buf, mode,
                                    reinterpret_cast<cudaStream_t>(stream), touch));
+}
+
+dd_status dd_gather_h2d_kv(const dd_shape* shape, const void* kv_host, const int32_t* idx,
+                           void* k_buf, void* v_buf, int mode, dd_stream_t stream) {
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  if (mode != 0 && mode != 1) return DD_ERR_UNSUPPORTED;
+  if (mode == 1 && !lsu_gather_fits(d)) return DD_ERR_UNSUPPORTED;
+  if (!kv_host || !idx || !k_buf || !v_buf) return DD_ERR_INVALID_ARG;
+  if (!aligned16(kv_host) || !aligned16(k_buf) || !aligned16(v_buf)) return DD_ERR_INVALID_ARG;
+  const void* kvh = host_to_device(kv_host);
+  if (!kvh) return DD_ERR_INVALID_ARG;
+  if (!all_device({idx, k_buf, v_buf})) return DD_ERR_INVALID_ARG;
+  const size_t rb = (size_t)d.d * d.elt;
+  const HostKV h{kvh, static_cast<const char*>(kvh) + rb, 2 * rb};
+  return cuda_status(launch_gather(d, h, idx, k_buf, v_buf, mode,
+                                   reinterpret_cast<cudaStream_t>(stream),
+                                   in_huge_page_store(kv_host)));
 }
 
 dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void* k_buf,
@@ -283,28 +303,30 @@ dd_status dd_sparse_decode_attn(const dd_shape* shape, const void* q, const void
                                  reinterpret_cast<cudaStream_t>(stream)));
 }
 
-dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_dev,
-                            const int32_t* idx_spec, const void* k_buf_spec,
-                            const void* v_buf_spec, const void* k_host, const void* v_host,
-                            int32_t* idx_true_out, void* k_buf_out, void* v_buf_out,
-                            int32_t* miss_out, float* mass_out, void* workspace, size_t ws_bytes,
-                            dd_stream_t stream) {
+}  // extern "C"
+
+namespace {
+// Miss correction against a host store described by `h` (rows already
+// translated to device-accessible addresses; h.k == NULL if the store was not
+// page-locked host memory).
+dd_status correct_misses(const dd_shape* shape, const void* q, const void* k_dev,
+                         const int32_t* idx_spec, const void* k_buf_spec, const void* v_buf_spec,
+                         const HostKV& h, int32_t* idx_true_out, void* k_buf_out,
+                         void* v_buf_out, int32_t* miss_out, float* mass_out, void* workspace,
+                         size_t ws_bytes, dd_stream_t stream) {
   Dims d;
   dd_status st = resolve(shape, &d);
   if (st != DD_OK) return st;
   if (d.k > kMaxCorrectK) return DD_ERR_UNSUPPORTED;
-  if (!q || !k_dev || !idx_spec || !k_buf_spec || !v_buf_spec || !k_host || !v_host ||
-      !idx_true_out || !k_buf_out || !v_buf_out || !workspace)
+  if (!q || !k_dev || !idx_spec || !k_buf_spec || !v_buf_spec || !idx_true_out || !k_buf_out ||
+      !v_buf_out || !workspace)
     return DD_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_dev) || !aligned16(k_buf_spec) || !aligned16(v_buf_spec) ||
-      !aligned16(k_host) || !aligned16(v_host) || !aligned16(k_buf_out) ||
-      !aligned16(v_buf_out) || !aligned16(workspace))
+      !aligned16(k_buf_out) || !aligned16(v_buf_out) || !aligned16(workspace))
     return DD_ERR_INVALID_ARG;
   const WsLayout w = ws_layout(d);
   if (ws_bytes < w.total) return DD_ERR_INVALID_ARG;
-  const void* kh = host_to_device(k_host);
-  const void* vh = host_to_device(v_host);
-  if (!kh || !vh) return DD_ERR_INVALID_ARG;
+  if (!h.k || !h.v) return DD_ERR_INVALID_ARG;
   if (!all_device({q, k_dev, idx_spec, k_buf_spec, v_buf_spec, idx_true_out, k_buf_out, v_buf_out,
                    miss_out, mass_out, workspace}))
     return DD_ERR_INVALID_ARG;
@@ -315,8 +337,45 @@ dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_
   st = cuda_status(
       select_rows(d, w, ws, q, k_dev, idx_true_out, sel_true, nullptr, false, s, &launches));
   if (st != DD_OK) return st;
-  return cuda_status(launch_fixup(d, idx_spec, idx_true_out, sel_true, k_buf_spec, v_buf_spec, kh,
-                                  vh, k_buf_out, v_buf_out, miss_out, mass_out, s));
+  return cuda_status(launch_fixup(d, idx_spec, idx_true_out, sel_true, k_buf_spec, v_buf_spec, h,
+                                  k_buf_out, v_buf_out, miss_out, mass_out, s));
+}
+}  // namespace
+
+extern "C" {
+
+dd_status dd_correct_misses(const dd_shape* shape, const void* q, const void* k_dev,
+                            const int32_t* idx_spec, const void* k_buf_spec,
+                            const void* v_buf_spec, const void* k_host, const void* v_host,
+                            int32_t* idx_true_out, void* k_buf_out, void* v_buf_out,
+                            int32_t* miss_out, float* mass_out, void* workspace, size_t ws_bytes,
+                            dd_stream_t stream) {
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  if (d.k > kMaxCorrectK) return DD_ERR_UNSUPPORTED;
+  if (!k_host || !v_host || !aligned16(k_host) || !aligned16(v_host)) return DD_ERR_INVALID_ARG;
+  const HostKV h{host_to_device(k_host), host_to_device(v_host), (size_t)d.d * d.elt};
+  return correct_misses(shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, h, idx_true_out,
+                        k_buf_out, v_buf_out, miss_out, mass_out, workspace, ws_bytes, stream);
+}
+
+dd_status dd_correct_misses_kv(const dd_shape* shape, const void* q, const void* k_dev,
+                               const int32_t* idx_spec, const void* k_buf_spec,
+                               const void* v_buf_spec, const void* kv_host,
+                               int32_t* idx_true_out, void* k_buf_out, void* v_buf_out,
+                               int32_t* miss_out, float* mass_out, void* workspace,
+                               size_t ws_bytes, dd_stream_t stream) {
+  Dims d;
+  dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return st;
+  if (d.k > kMaxCorrectK) return DD_ERR_UNSUPPORTED;
+  if (!kv_host || !aligned16(kv_host)) return DD_ERR_INVALID_ARG;
+  const size_t rb = (size_t)d.d * d.elt;
+  const void* kvh = host_to_device(kv_host);
+  const HostKV h{kvh, kvh ? static_cast<const char*>(kvh) + rb : nullptr, 2 * rb};
+  return correct_misses(shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, h, idx_true_out,
+                        k_buf_out, v_buf_out, miss_out, mass_out, workspace, ws_bytes, stream);
 }
 
 dd_status dd_landmarks_size(const dd_shape* shape, int chunk, size_t* bytes) {
@@ -666,24 +725,35 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
   if (cudaGetDevice(&cur_dev) != cudaSuccess || cur_dev != c->device) return DD_ERR_INVALID_ARG;
   const Dims& d = c->dims;
   // Synchronous checks of every layer before anything is enqueued.
-  std::vector<const void*> kh(n_layers), vh(n_layers);
+  std::vector<HostKV> hkv(n_layers);
   std::vector<char> touch(n_layers);
+  const size_t rb = (size_t)d.d * d.elt;
   // Without DD_STEP_LANDMARKS the key cache is scored, so k_dev is required;
   // with it, k_dev is needed only for the window's keys, if k_win is NULL.
   const bool lm_flag = (flags & DD_STEP_LANDMARKS) != 0;
   for (int l = 0; l < n_layers; ++l) {
     const dd_layer_io& io = layers[l];
-    if (!io.q_spec || !io.q || !io.k_host || !io.v_host || !io.out) return DD_ERR_INVALID_ARG;
+    if (!io.q_spec || !io.q || !io.out) return DD_ERR_INVALID_ARG;
+    // The host store: separate K and V stores, or one interleaved store.
+    if (io.kv_host ? (io.k_host || io.v_host) : (!io.k_host || !io.v_host))
+      return DD_ERR_INVALID_ARG;
     if (!io.k_dev && !(lm_flag && (io.k_win || d.W == 0))) return DD_ERR_INVALID_ARG;
     if (d.W > 0 && !io.v_win) return DD_ERR_INVALID_ARG;
     if (!aligned16(io.q_spec) || !aligned16(io.q) || !aligned16(io.k_dev) ||
-        !aligned16(io.k_host) || !aligned16(io.v_host) || !aligned16(io.out) ||
+        !aligned16(io.k_host) || !aligned16(io.v_host) || !aligned16(io.kv_host) ||
+        !aligned16(io.out) ||
         !aligned16(io.v_win) || !aligned16(io.k_win))
       return DD_ERR_INVALID_ARG;
-    kh[l] = host_to_device(io.k_host);
-    vh[l] = host_to_device(io.v_host);
-    if (!kh[l] || !vh[l]) return DD_ERR_INVALID_ARG;
-    touch[l] = in_huge_page_store(io.k_host) || in_huge_page_store(io.v_host);
+    if (io.kv_host) {
+      const void* kvh = host_to_device(io.kv_host);
+      if (!kvh) return DD_ERR_INVALID_ARG;
+      hkv[l] = HostKV{kvh, static_cast<const char*>(kvh) + rb, 2 * rb};
+      touch[l] = in_huge_page_store(io.kv_host);
+    } else {
+      hkv[l] = HostKV{host_to_device(io.k_host), host_to_device(io.v_host), rb};
+      if (!hkv[l].k || !hkv[l].v) return DD_ERR_INVALID_ARG;
+      touch[l] = in_huge_page_store(io.k_host) || in_huge_page_store(io.v_host);
+    }
     if (!all_device({io.q_spec, io.q, io.k_dev, io.v_win, io.k_win, io.out}))
       return DD_ERR_INVALID_ARG;
   }
@@ -791,8 +861,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       if (e != cudaSuccess) return e;
     }
     if (phases) cudaEventRecord(T(l, PH_GATHER0), X);
-    e = launch_gather(d, kh[l], vh[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X,
-                      touch[l]);
+    e = launch_gather(d, hkv[l], c->idx[s], c->kbuf[s], c->vbuf[s], gather_mode, X, touch[l]);
     if (e != cudaSuccess) return e;
     if (phases) cudaEventRecord(T(l, PH_GATHER1), X);
     launches += kGatherLaunches - (touch[l] ? 0 : 1);
@@ -823,7 +892,7 @@ dd_status dd_decode_step(dd_ctx* c, const dd_layer_io* layers, int n_layers,
       e = select_rows(d, c->ws_lay, ws, layers[l].q, layers[l].k_dev, c->idx_true, sel_true,
                       nullptr, fused, A, &launches);
       if (e == cudaSuccess)
-        e = launch_fixup(d, c->idx[s], c->idx_true, sel_true, c->kbuf[s], c->vbuf[s], kh[l], vh[l],
+        e = launch_fixup(d, c->idx[s], c->idx_true, sel_true, c->kbuf[s], c->vbuf[s], hkv[l],
                          c->kb_true, c->vb_true, c->miss + (size_t)l * d.U,
                          c->mass + (size_t)l * d.U * 2, A);
       if (e != cudaSuccess) return e;

@@ -29,7 +29,7 @@ __global__ void __launch_bounds__(kFixThreads)
                  const uint4* __restrict__ vb_spec, const uint4* __restrict__ k_host,
                  const uint4* __restrict__ v_host, uint4* __restrict__ kb_out,
                  uint4* __restrict__ vb_out, int32_t* __restrict__ miss_out,
-                 float* __restrict__ mass_out, int n, int k) {
+                 float* __restrict__ mass_out, int n, int k, int hsp) {
   extern __shared__ int32_t src[];  // slot of the prefetched buffer, or -(1 + host position)
   __shared__ int red_i[kFixThreads / 32];
   __shared__ float red_h[kFixThreads / 32], red_a[kFixThreads / 32];
@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(kFixThreads)
           v[r] = ld_ro((t ? vb_spec : kb_spec) + ((size_t)u * k + s) * CPR + part);
         } else {
           const int j = min(max(-s - 1, 0), n - 1);  // never outside the store
-          v[r] = ld_ro((t ? v_host : k_host) + ((size_t)u * n + j) * CPR + part);
+          v[r] = ld_ro((t ? v_host : k_host) + ((size_t)u * n + j) * hsp + part);
         }
       }
     }
@@ -115,17 +115,17 @@ __global__ void __launch_bounds__(kFixThreads)
 template <int CPR>
 cudaError_t launch_fix(const Dims& d, const int32_t* idx_spec, const int32_t* idx_true,
                        const float* sel_true, const void* kb_spec, const void* vb_spec,
-                       const void* k_host, const void* v_host, void* kb_out, void* vb_out,
-                       int32_t* miss_out, float* mass_out, cudaStream_t st) {
+                       const HostKV& h, void* kb_out, void* vb_out, int32_t* miss_out,
+                       float* mass_out, cudaStream_t st) {
   static unsigned long long prepared = 0;
   const int smem = d.k * (int)sizeof(int32_t);
   cudaError_t e = prepare_kernel(fixup_kernel<CPR>, &prepared, kMaxCorrectK * (int)sizeof(int32_t));
   if (e != cudaSuccess) return e;
   fixup_kernel<CPR><<<d.U, kFixThreads, smem, st>>>(
       idx_spec, idx_true, sel_true, static_cast<const uint4*>(kb_spec),
-      static_cast<const uint4*>(vb_spec), static_cast<const uint4*>(k_host),
-      static_cast<const uint4*>(v_host), static_cast<uint4*>(kb_out), static_cast<uint4*>(vb_out),
-      miss_out, mass_out, d.n, d.k);
+      static_cast<const uint4*>(vb_spec), static_cast<const uint4*>(h.k),
+      static_cast<const uint4*>(h.v), static_cast<uint4*>(kb_out), static_cast<uint4*>(vb_out),
+      miss_out, mass_out, d.n, d.k, (int)(h.hs / 16));
   return cudaGetLastError();
 }
 
@@ -133,12 +133,12 @@ cudaError_t launch_fix(const Dims& d, const int32_t* idx_spec, const int32_t* id
 
 cudaError_t launch_fixup(const Dims& d, const int32_t* idx_spec, const int32_t* idx_true,
                          const float* sel_true, const void* kb_spec, const void* vb_spec,
-                         const void* k_host, const void* v_host, void* kb_out, void* vb_out,
-                         int32_t* miss_out, float* mass_out, cudaStream_t st) {
+                         const HostKV& h, void* kb_out, void* vb_out, int32_t* miss_out,
+                         float* mass_out, cudaStream_t st) {
   switch (d.d * d.elt / 16) {
-    case 8: return launch_fix<8>(d, idx_spec, idx_true, sel_true, kb_spec, vb_spec, k_host, v_host, kb_out, vb_out, miss_out, mass_out, st);
-    case 16: return launch_fix<16>(d, idx_spec, idx_true, sel_true, kb_spec, vb_spec, k_host, v_host, kb_out, vb_out, miss_out, mass_out, st);
-    case 32: return launch_fix<32>(d, idx_spec, idx_true, sel_true, kb_spec, vb_spec, k_host, v_host, kb_out, vb_out, miss_out, mass_out, st);
+    case 8: return launch_fix<8>(d, idx_spec, idx_true, sel_true, kb_spec, vb_spec, h, kb_out, vb_out, miss_out, mass_out, st);
+    case 16: return launch_fix<16>(d, idx_spec, idx_true, sel_true, kb_spec, vb_spec, h, kb_out, vb_out, miss_out, mass_out, st);
+    case 32: return launch_fix<32>(d, idx_spec, idx_true, sel_true, kb_spec, vb_spec, h, kb_out, vb_out, miss_out, mass_out, st);
   }
   return cudaErrorInvalidValue;
 }

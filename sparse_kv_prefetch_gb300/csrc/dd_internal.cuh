@@ -49,11 +49,20 @@ cudaError_t launch_score_bf16_query(const Dims& d, const void* q_bf16, const voi
 cudaError_t launch_score_select(const Dims& d, const void* q_spec, const void* k_dev,
                                 float* logits, float2* part, int32_t* counters, int32_t* idx,
                                 float* sel, float* lse, cudaStream_t st);
+// Where the host store's rows are, as device-accessible addresses: position j
+// of unit u has its K row at k + (u n + j) hs and its V row at v + (u n + j) hs
+// bytes.  hs is the row's bytes for separate K and V stores; for one store
+// holding each position's K row followed by its V row, v = k + row bytes and
+// hs = twice the row bytes.
+struct HostKV {
+  const void* k;
+  const void* v;
+  size_t hs;
+};
 // touch: first read one word per huge page of the host stores (worth it only
 // for stores backed by huge pages, i.e. from dd_host_alloc).
-cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
-                          const int32_t* idx, void* k_buf, void* v_buf, int mode,
-                          cudaStream_t st, bool touch);
+cudaError_t launch_gather(const Dims& d, const HostKV& h, const int32_t* idx, void* k_buf,
+                          void* v_buf, int mode, cudaStream_t st, bool touch);
 // Geometry of the bulk-copy gather (mode 0), process-wide: grid in percent
 // of the SM count, bytes per tensor of a shared-memory stage, stages per CTA.
 dd_status set_gather_geometry(int grid_pct, int tile_bytes, int stages);
@@ -99,8 +108,8 @@ cudaError_t launch_attn(const Dims& d, const void* q, const void* k_buf, const v
 constexpr int kMaxCorrectK = 4096;
 cudaError_t launch_fixup(const Dims& d, const int32_t* idx_spec, const int32_t* idx_true,
                          const float* sel_true, const void* kb_spec, const void* vb_spec,
-                         const void* k_host, const void* v_host, void* kb_out, void* vb_out,
-                         int32_t* miss_out, float* mass_out, cudaStream_t st);
+                         const HostKV& h, void* kb_out, void* vb_out, int32_t* miss_out,
+                         float* mass_out, cudaStream_t st);
 
 // Landmark selection (landmark.cu).
 cudaError_t launch_landmarks(const Dims& d, int chunk, const void* k_dev, float* landmarks,

@@ -91,9 +91,10 @@ __global__ void __launch_bounds__(32)
     gather_tma_kernel(const unsigned char* __restrict__ k_host,
                       const unsigned char* __restrict__ v_host, const int32_t* __restrict__ idx,
                       unsigned char* __restrict__ k_buf, unsigned char* __restrict__ v_buf, int n,
-                      int k, int units, int R, int stages) {
+                      int k, int units, int R, int stages, size_t hs) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tile_bytes = R * RB;
+  const bool runs = hs == RB;  // consecutive positions are contiguous in the store
   unsigned char* ring_k = smem;
   unsigned char* ring_v = smem + (size_t)stages * tile_bytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)2 * stages * tile_bytes);
@@ -108,9 +109,9 @@ __global__ void __launch_bounds__(32)
   __syncwarp();
 
   // Issue the row copies of `tile` into stage s.  Rows whose positions are
-  // consecutive (whole chunks under landmark selection) are contiguous in the
-  // host store and in the tile, so each run of them is one bulk copy: the
-  // lane holding the first row of a run copies the run.
+  // consecutive (whole chunks under landmark selection) are contiguous in a
+  // store of separate K and V rows and in the tile, so each run of them is
+  // one bulk copy: the lane holding the first row of a run copies the run.
   auto issue = [&](int tile, int s) {
     const int u = tile / tiles_per_unit, i0 = (tile - u * tiles_per_unit) * R;
     const int nr = min(R, k - i0);
@@ -122,12 +123,12 @@ __global__ void __launch_bounds__(32)
       int j = 0;
       if (valid) j = min(max(__ldg(idx + (size_t)u * k + i0 + r), 0), n - 1);  // never outside
       const int jp = __shfl_up_sync(0xffffffffu, j, 1);
-      const bool cont = valid && lane > 0 && jp + 1 == j;  // continues the run before it
+      const bool cont = runs && valid && lane > 0 && jp + 1 == j;  // continues the run before it
       const unsigned cmask = __ballot_sync(0xffffffffu, cont);
       if (valid && !cont) {
         const unsigned after = lane == 31 ? 0u : cmask >> (lane + 1);
         const int len = __ffs(~after);  // this row plus the continuing rows after it
-        const size_t src = ((size_t)u * n + j) * RB;
+        const size_t src = ((size_t)u * n + j) * hs;
         const uint32_t bytes = (uint32_t)(len * RB);
         // Host lines are read once: evict them first, so they do not push the
         // scoring kernel's logits out of L2.
@@ -177,8 +178,8 @@ __global__ void __launch_bounds__(32)
 }
 
 template <int RB>
-cudaError_t launch_tma(const Dims& d, const void* kh, const void* vh, const int32_t* idx,
-                       void* kb, void* vb, cudaStream_t st) {
+cudaError_t launch_tma(const Dims& d, const HostKV& h, const int32_t* idx, void* kb, void* vb,
+                       cudaStream_t st) {
   static unsigned long long prepared = 0;
   cudaError_t e = prepare_kernel(gather_tma_kernel<RB>, &prepared, kMaxDynSmem);
   if (e != cudaSuccess) return e;
@@ -189,9 +190,9 @@ cudaError_t launch_tma(const Dims& d, const void* kh, const void* vh, const int3
   if (grid > tiles) grid = tiles;
   if (grid < 1) grid = 1;
   gather_tma_kernel<RB><<<(unsigned)grid, 32, tma_smem(R, RB, stages), st>>>(
-      static_cast<const unsigned char*>(kh), static_cast<const unsigned char*>(vh), idx,
+      static_cast<const unsigned char*>(h.k), static_cast<const unsigned char*>(h.v), idx,
       static_cast<unsigned char*>(kb), static_cast<unsigned char*>(vb), d.n, d.k, d.U, R,
-      stages);
+      stages, h.hs);
   return cudaGetLastError();
 }
 
@@ -211,7 +212,7 @@ __device__ __forceinline__ void gather_lsu_body(const uint4* __restrict__ k_host
                                                 const int32_t* __restrict__ idx,
                                                 uint4* __restrict__ k_buf,
                                                 uint4* __restrict__ v_buf, int n, int k,
-                                                long long rows) {
+                                                long long rows, long long hsp) {
   // Piece p of the flattened work list: row r = p / (2 CPR), tensor t (K or
   // V) = (p / CPR) & 1, part = p % CPR.  Consecutive threads read consecutive
   // pieces of a row.  Host lines are read once: streaming loads.
@@ -233,7 +234,7 @@ __device__ __forceinline__ void gather_lsu_body(const uint4* __restrict__ k_host
         const int part = (int)(p % CPR);
         const unsigned u = r / (unsigned)k;
         const int j = min(max(__ldg(idx + r), 0), n - 1);  // never read outside the store
-        const uint4* src = (t ? v_host : k_host) + (((long long)u * n + j) * CPR + part);
+        const uint4* src = (t ? v_host : k_host) + (((long long)u * n + j) * hsp + part);
         v[i] = ld_stream(src);
         dst[i] = (int)(((unsigned)r * CPR + part) * 2u + t);
       }
@@ -248,13 +249,13 @@ template <int CPR>
 __global__ void __launch_bounds__(kLsuMaxThreads)
     gather_lsu_kernel(const uint4* __restrict__ k_host, const uint4* __restrict__ v_host,
                       const int32_t* __restrict__ idx, uint4* __restrict__ k_buf,
-                      uint4* __restrict__ v_buf, int n, int k, long long rows) {
-  gather_lsu_body<CPR, kInFlight>(k_host, v_host, idx, k_buf, v_buf, n, k, rows);
+                      uint4* __restrict__ v_buf, int n, int k, long long rows, long long hsp) {
+  gather_lsu_body<CPR, kInFlight>(k_host, v_host, idx, k_buf, v_buf, n, k, rows, hsp);
 }
 
 template <int CPR>
-cudaError_t launch_lsu(const Dims& d, const void* kh, const void* vh, const int32_t* idx,
-                       void* kb, void* vb, cudaStream_t st) {
+cudaError_t launch_lsu(const Dims& d, const HostKV& h, const int32_t* idx, void* kb, void* vb,
+                       cudaStream_t st) {
   static unsigned long long prepared = 0;
   const long long rows = (long long)d.U * d.k;
   if (rows * 2 * CPR * 2 >= (1ll << 31)) return cudaErrorInvalidValue;  // piece index range
@@ -267,16 +268,16 @@ cudaError_t launch_lsu(const Dims& d, const void* kh, const void* vh, const int3
   if (grid > work) grid = work;
   if (grid < 1) grid = 1;
   gather_lsu_kernel<CPR><<<(unsigned)grid, threads, 0, st>>>(
-      static_cast<const uint4*>(kh), static_cast<const uint4*>(vh), idx,
-      static_cast<uint4*>(kb), static_cast<uint4*>(vb), d.n, d.k, rows);
+      static_cast<const uint4*>(h.k), static_cast<const uint4*>(h.v), idx,
+      static_cast<uint4*>(kb), static_cast<uint4*>(vb), d.n, d.k, rows,
+      (long long)(h.hs / 16));
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
-                          const int32_t* idx, void* k_buf, void* v_buf, int mode,
-                          cudaStream_t st, bool touch) {
+cudaError_t launch_gather(const Dims& d, const HostKV& h, const int32_t* idx, void* k_buf,
+                          void* v_buf, int mode, cudaStream_t st, bool touch) {
   const int rb = d.d * d.elt;
   if (touch && (mode == 0 || mode == 1)) {
     static unsigned int* sinks[64] = {};  // device address of g_touch_sink, per device
@@ -288,24 +289,26 @@ cudaError_t launch_gather(const Dims& d, const void* k_host, const void* v_host,
       e0 = cudaGetSymbolAddress(reinterpret_cast<void**>(&sink), g_touch_sink);
       if (e0 != cudaSuccess) return e0;
     }
-    const size_t bytes = (size_t)d.U * d.n * rb;
-    touch_pages_kernel<<<1, 32, 0, st>>>(static_cast<const unsigned char*>(k_host),
-                                         static_cast<const unsigned char*>(v_host), bytes,
+    // The rows span U n hs bytes from each base (the two ranges overlap in an
+    // interleaved store, which touches its pages twice: harmless).
+    const size_t bytes = (size_t)d.U * d.n * h.hs - (h.hs - rb);
+    touch_pages_kernel<<<1, 32, 0, st>>>(static_cast<const unsigned char*>(h.k),
+                                         static_cast<const unsigned char*>(h.v), bytes,
                                          host_page_bytes(), sink);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (mode == 0) {
     switch (rb) {
-      case 128: return launch_tma<128>(d, k_host, v_host, idx, k_buf, v_buf, st);
-      case 256: return launch_tma<256>(d, k_host, v_host, idx, k_buf, v_buf, st);
-      case 512: return launch_tma<512>(d, k_host, v_host, idx, k_buf, v_buf, st);
+      case 128: return launch_tma<128>(d, h, idx, k_buf, v_buf, st);
+      case 256: return launch_tma<256>(d, h, idx, k_buf, v_buf, st);
+      case 512: return launch_tma<512>(d, h, idx, k_buf, v_buf, st);
     }
   } else if (mode == 1) {
     switch (rb / 16) {
-      case 8: return launch_lsu<8>(d, k_host, v_host, idx, k_buf, v_buf, st);
-      case 16: return launch_lsu<16>(d, k_host, v_host, idx, k_buf, v_buf, st);
-      case 32: return launch_lsu<32>(d, k_host, v_host, idx, k_buf, v_buf, st);
+      case 8: return launch_lsu<8>(d, h, idx, k_buf, v_buf, st);
+      case 16: return launch_lsu<16>(d, h, idx, k_buf, v_buf, st);
+      case 32: return launch_lsu<32>(d, h, idx, k_buf, v_buf, st);
     }
   }
   return cudaErrorInvalidValue;
