@@ -17,7 +17,15 @@
 // and the lane that owns a row writes its logit and folds it into a running
 // (max, sum of exp).  All query heads of a GQA group are scored from the same
 // K row.  With FUSED, the unit's last CTA also runs its top-k (select.cuh).
+//
+// bf16 keys scored by a group of two or more query heads take the tensor
+// cores instead: the group's heads times a 16-row tile of keys is a small
+// matrix product, which one warp-level mma per 16 elements of the row
+// computes with fp32 accumulation, so the FMA and widening instructions that
+// make the per-lane form issue-bound disappear (see the consumer below).
 #include <math.h>
+
+#include <type_traits>
 
 #include "dd_internal.cuh"
 #include "select.cuh"
@@ -55,24 +63,66 @@ struct ScoreGeom {
   static_assert(kStageRows % kGroups == 0, "stage must hold whole row groups");
 };
 
+// Whether a layout is scored on the tensor cores: bf16 keys, a group of two
+// or more query heads, bf16 query.
+template <typename T, int G, bool QB>
+__host__ __device__ constexpr bool use_mma() {
+  return std::is_same<T, bf16_t>::value && G >= 2 && !QB;
+}
+// The tensor-core consumer reads each key row as four lanes' 16-byte pieces.
+// Rows start on 128-byte bank boundaries, so two rows at the same piece meet
+// in the same banks.  Its stages are therefore filled as two halves with the
+// second 64 bytes further on: a warp's loads then always pair a row of one
+// half with a row of the other and touch every bank once.
+constexpr int kHalfSkew = 64;
+template <bool MMA>
+__host__ __device__ constexpr int stage_stride() {
+  return MMA ? kStageBytes + kHalfSkew : kStageBytes;
+}
+
 // Fused selection: the last CTA of a unit to finish runs the unit's top-k
 // with its eight consumer warps, reusing the ring's shared memory.
 constexpr int kSelWarps = kConsumerWarps;
 constexpr int kSelCap = 1024;  // list entries per warp
 using SelSmem = sel::Smem<kSelWarps, kSelCap>;
-constexpr size_t kRingBytes = (size_t)kStages * kStageBytes;
+template <bool MMA>
+__host__ __device__ constexpr size_t ring_bytes() {
+  return (size_t)kStages * stage_stride<MMA>();
+}
 // Dynamic shared memory: [0, region): the ring (and, when FUSED, later the
 // selection's lists, which need more); then the mbarriers.  The plain kernel
 // asks only for the ring, so that three of its CTAs leave room on an SM for a
 // gather CTA running beside them.
-template <bool FUSED>
+template <bool FUSED, bool MMA>
 __host__ __device__ constexpr size_t region_bytes() {
-  return ((FUSED && sizeof(SelSmem) > kRingBytes ? sizeof(SelSmem) : kRingBytes) + 127) / 128 *
-         128;
+  return ((FUSED && sizeof(SelSmem) > ring_bytes<MMA>() ? sizeof(SelSmem) : ring_bytes<MMA>()) +
+          127) / 128 * 128;
 }
-template <bool FUSED>
+template <bool FUSED, bool MMA>
 __host__ __device__ constexpr size_t score_smem() {
-  return region_bytes<FUSED>() + 2 * kStages * sizeof(uint64_t);
+  return region_bytes<FUSED, MMA>() + 2 * kStages * sizeof(uint64_t);
+}
+
+// D[16x8] += A[16x16] B[16x8] on the tensor cores, bf16 inputs, fp32
+// accumulation.  Fragments (g = lane / 4, c = lane % 4): a0 = A[g][2c..2c+1],
+// a1 = A[g+8][2c..2c+1], a2 = A[g][2c+8..2c+9], a3 = A[g+8][2c+8..2c+9];
+// b0 = B[2c..2c+1][g], b1 = B[2c+8..2c+9][g]; d = D[g][2c..2c+1],
+// D[g+8][2c..2c+1].  Each register holds two bf16, the lower k in the low half.
+__device__ __forceinline__ void mma_16x8x16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                            uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// Fold logit sv into a running (max, sum of exp) with one exponential: a new
+// maximum rescales the sum, any other logit adds its term.
+__device__ __forceinline__ void online_lse(float sv, float& m_run, float& l_run) {
+  const float dv = sv - m_run;
+  const float ev = __expf(-fabsf(dv));
+  l_run = dv > 0.f ? fmaf(l_run, ev, 1.f) : l_run + ev;
+  m_run = fmaxf(m_run, sv);
 }
 
 // Selection outputs of the fused kernel (unused when FUSED is false).
@@ -87,7 +137,7 @@ struct FusedOut {
 // QB: the keys are fp32 (landmarks) but the query is bf16; it is widened
 // exactly on load.
 template <typename T, int D, int G, bool FUSED, bool QB = false>
-__global__ void __launch_bounds__(kScoreThreads)
+__global__ void __launch_bounds__(kScoreThreads, use_mma<T, G, QB>() && !FUSED ? 3 : 1)
     score_kernel(const uint4* __restrict__ q_spec, const unsigned char* __restrict__ K,
                  float* __restrict__ logits, float2* __restrict__ part, int n, int ldn, int Hq,
                  int Hkv, int chunk, int nchunks, float scale, FusedOut fo) {
@@ -98,10 +148,13 @@ __global__ void __launch_bounds__(kScoreThreads)
   constexpr int S = ilog2(N) < ilog2(LPR) ? ilog2(N) : ilog2(LPR);  // transposing steps
   constexpr int P = N >> S;                      // totals per lane after the reduction
   static_assert(P <= RPG && RPG % P == 0, "a lane's totals must share one head");
+  constexpr bool MMA = use_mma<T, G, QB>();
+  constexpr int STRIDE = stage_stride<MMA>();
+  constexpr int HALF = SR / 2;  // rows in each half of a stage (tensor-core form)
 
   extern __shared__ __align__(128) unsigned char smem[];
   unsigned char* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + region_bytes<FUSED>());
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + region_bytes<FUSED, MMA>());
   uint64_t* empty = full + kStages;
 
   const int item = blockIdx.x;
@@ -121,9 +174,10 @@ __global__ void __launch_bounds__(kScoreThreads)
   }
   __syncthreads();
 
-  // Running (max, sum of exp) of the logits this lane writes (one head).
-  float m_run = -INFINITY, l_run = 0.f;
-  int head = -1;  // the lane's head; -1 for lanes that write nothing
+  // Running (max, sum of exp) of the logits this lane writes: heads head0
+  // and, in the tensor-core form, head0 + 1 (head0 = -1: the lane writes none).
+  float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};
+  int head0 = -1;
   bool ok = true;
   const unsigned char* Ku = K + (size_t)u * n * RB;
 
@@ -141,9 +195,88 @@ __global__ void __launch_bounds__(kScoreThreads)
         }
         const int r0 = j_begin + t * SR;
         const int nr = min(SR, j_end - r0);
+        unsigned char* dst = ring + (size_t)s * STRIDE;
         mbar_arrive_expect_tx(&full[s], (uint32_t)(nr * RB));
-        bulk_load_hint(ring + (size_t)s * kStageBytes, Ku + (size_t)r0 * RB,
-                       (uint32_t)(nr * RB), &full[s], policy);
+        if constexpr (MMA) {  // two halves, the second kHalfSkew bytes on
+          const int na = min(nr, HALF);
+          bulk_load_hint(dst, Ku + (size_t)r0 * RB, (uint32_t)(na * RB), &full[s], policy);
+          if (nr > HALF)
+            bulk_load_hint(dst + HALF * RB + kHalfSkew, Ku + (size_t)(r0 + HALF) * RB,
+                           (uint32_t)((nr - HALF) * RB), &full[s], policy);
+        } else {
+          bulk_load_hint(dst, Ku + (size_t)r0 * RB, (uint32_t)(nr * RB), &full[s], policy);
+        }
+      }
+    }
+  } else if constexpr (MMA) {
+    // Tensor-core consumer.  A stage is TPS tiles of 16 rows; tile tau holds
+    // rows tau*8 .. tau*8+7 of each half, the even mma rows from the first
+    // half and the odd ones from the second (mma row m: half m & 1, row
+    // tau*8 + m/2), and the stage's tiles go to the warps in turn.  The mma's
+    // A operand is the tile of keys, its B operand the group's query heads
+    // (columns G..7 zero).  The contraction over the d elements of a row is
+    // taken in blocks of 32: lane (g, c) loads the 16-byte piece c of block
+    // bb of its rows g and g+8 (A) and of query head g (B), and both operands
+    // map the eight elements of a piece to the same logical k of two mmas
+    // (elements 0-1 -> k 2c..2c+1 and 2-3 -> k 2c+8..2c+9 of the first mma,
+    // elements 4-7 likewise of the second), so every element of the row
+    // meets its query element exactly once.
+    constexpr int TPS = SR / 16;
+    constexpr int NB = D / 32;
+    static_assert(SR % 16 == 0 && TPS <= kConsumerWarps && kConsumerWarps % TPS == 0,
+                  "a stage must split into whole tiles, at most one per warp");
+    static_assert(RB % 128 == 0, "rows must start on bank boundaries");
+    const int gq = lane >> 2, cq = lane & 3;
+    uint4 qb[NB];
+#pragma unroll
+    for (int bb = 0; bb < NB; ++bb)
+      qb[bb] = gq < G ? ld_ro(q_spec + (size_t)(b * Hq + hk * G + gq) * (D / 8) + 4 * bb + cq)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    if (2 * cq < G) head0 = 2 * cq;  // accumulator columns 2c, 2c+1 are heads
+    const int par = gq & 1, hr = gq >> 1;
+    // Byte offsets in a stage of the lane's piece of rows g and g+8 of tile 0.
+    const int off0 = (par ? HALF * RB + kHalfSkew : 0) + hr * RB + 16 * cq;
+    const int off1 = off0 + 4 * RB;
+    float* lg = logits + (size_t)(b * Hq + hk * G + (head0 < 0 ? 0 : head0)) * ldn;
+
+    for (int t = 0; t < n_stages; ++t) {
+      const int s = t % kStages;
+      if (!mbar_wait(&full[s], (t / kStages) & 1)) {
+        ok = false;
+        break;
+      }
+      const int tau = warp - ((t * TPS) & (kConsumerWarps - 1));
+      const bool mine = tau >= 0 && tau < TPS;
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      if (mine) {
+        const unsigned char* base = ring + (size_t)s * STRIDE + tau * 8 * RB;
+#pragma unroll
+        for (int bb = 0; bb < NB; ++bb) {
+          const uint4 a0 = *reinterpret_cast<const uint4*>(base + off0 + 64 * bb);
+          const uint4 a1 = *reinterpret_cast<const uint4*>(base + off1 + 64 * bb);
+          mma_16x8x16(acc, a0.x, a1.x, a0.y, a1.y, qb[bb].x, qb[bb].y);
+          mma_16x8x16(acc, a0.z, a1.z, a0.w, a1.w, qb[bb].z, qb[bb].w);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);  // the stage may be refilled
+      if (mine && head0 >= 0) {
+        const int j0 = j_begin + t * SR + par * HALF + tau * 8 + hr;  // mma row g
+        const int j1 = j0 + 4;                                          // mma row g + 8
+        if (j0 < j_end) {
+          const float s0 = acc[0] * scale, s1 = acc[1] * scale;
+          lg[j0] = s0;
+          lg[ldn + j0] = s1;
+          online_lse(s0, m_run[0], l_run[0]);
+          online_lse(s1, m_run[1], l_run[1]);
+        }
+        if (j1 < j_end) {
+          const float s2 = acc[2] * scale, s3 = acc[3] * scale;
+          lg[j1] = s2;
+          lg[ldn + j1] = s3;
+          online_lse(s2, m_run[0], l_run[0]);
+          online_lse(s3, m_run[1], l_run[1]);
+        }
       }
     }
   } else {
@@ -190,7 +323,7 @@ __global__ void __launch_bounds__(kScoreThreads)
     const int prefix = X / P;
     const int g_lane = X / RPG;
     const bool writer = (sub >> S) == 0;
-    if (writer) head = g_lane;
+    if (writer) head0 = g_lane;
     float* lg_row = logits + (size_t)(b * Hq + hk * G + g_lane) * ldn;
 
     for (int t = 0; t < n_stages; ++t) {
@@ -199,7 +332,7 @@ __global__ void __launch_bounds__(kScoreThreads)
         ok = false;
         break;
       }
-      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * kStageBytes);
+      const uint4* st = reinterpret_cast<const uint4*>(ring + (size_t)s * STRIDE);
       const int r0 = j_begin + t * SR;
       // Stage row (i * NG + grp), for i < RPG, belongs to this lane group.
       float acc[N];
@@ -251,12 +384,7 @@ __global__ void __launch_bounds__(kScoreThreads)
           if (j < j_end) {
             const float sv = acc[p] * scale;
             lg_row[j] = sv;
-            // Online (max, sum of exp) with one exponential: a new maximum
-            // rescales the sum, any other logit adds its term.
-            const float dv = sv - m_run;
-            const float ev = __expf(-fabsf(dv));
-            l_run = dv > 0.f ? fmaf(l_run, ev, 1.f) : l_run + ev;
-            m_run = fmaxf(m_run, sv);
+            online_lse(sv, m_run[0], l_run[0]);
           }
         }
       }
@@ -276,7 +404,9 @@ __global__ void __launch_bounds__(kScoreThreads)
   __shared__ float2 red[G][kConsumerWarps + 1];
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    float2 p = head == g ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
+    float2 p = make_float2(-INFINITY, 0.f);
+    if (head0 >= 0 && g == head0) p = make_float2(m_run[0], l_run[0]);
+    if (MMA && head0 >= 0 && g == head0 + 1) p = make_float2(m_run[1], l_run[1]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       float2 o;
@@ -320,7 +450,7 @@ template <typename T, int D, int G, bool FUSED, bool QB = false>
 cudaError_t launch_typed(const Dims& d, const void* q_spec, const void* k_dev, float* logits,
                          float2* part, const FusedOut& fo, cudaStream_t st) {
   static unsigned long long prepared = 0;
-  constexpr size_t smem_bytes = score_smem<FUSED>();
+  constexpr size_t smem_bytes = score_smem<FUSED, use_mma<T, G, QB>()>();
   cudaError_t e = prepare_kernel(score_kernel<T, D, G, FUSED, QB>, &prepared, (int)smem_bytes);
   if (e != cudaSuccess) return e;
   const float scale = 1.0f / sqrtf((float)d.d);
