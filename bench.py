@@ -53,11 +53,11 @@ UNIT = "layer-steps/s"
 FALLBACK_HBM_GBS = 6800.0
 # DRAM read + write bytes of one scoring launch, from ncu captures of the
 # current kernel (profiles/), scaled by units to the full layer.  GQA-128K: a
-# batch-16 capture (128 units: 4.2957 GB read, 0.2134 GB of logits written,
-# mean of two launches) doubled for the 256 units of the layer.  Keyed by
-# (workload, top-k fused into the scoring kernel); absent where no capture of
-# the current kernel exists.
-SCORE_TRAFFIC_BYTES = {("c5-gqa-128k", False): 2 * (4295654912 + 213407360)}
+# batch-16 capture of the tensor-core form (128 units: 4.2954 GB read,
+# 0.2204 GB of logits written, mean of two launches) doubled for the 256 units
+# of the layer.  Keyed by (workload, top-k fused into the scoring kernel);
+# absent where no capture of the current kernel exists.
+SCORE_TRAFFIC_BYTES = {("c5-gqa-128k", False): 2 * (4295449856 + 220422528)}
 
 
 def parse():
@@ -127,9 +127,14 @@ def parse():
 # Gather variants the calibration tries: (tag, mode, geometry).  The small
 # bulk-copy geometry fits beside the scoring kernel; the wide one keeps 5x the
 # rows in flight, which pays on stores of small pages (translation latency);
-# the load/store gather (eight warps per SM) takes no shared memory.
+# the half one keeps half the small one's rows in flight on half the SMs: on a
+# store whose gather is bound by address translation, rows in flight beyond
+# what the translations admit only wait, and they hold memory-system slots the
+# scoring beside them needs; the load/store gather (eight warps per SM) takes
+# no shared memory.
 GATHER_VARIANTS = (("bulk_copy_small", 0, (100, 4096, 3)),
                    ("bulk_copy_wide", 0, (200, 8192, 4)),
+                   ("bulk_copy_half", 0, (50, 4096, 3)),
                    ("load_store", 1, (100, 256)))
 
 

@@ -18,11 +18,12 @@
 // (max, sum of exp).  All query heads of a GQA group are scored from the same
 // K row.  With FUSED, the unit's last CTA also runs its top-k (select.cuh).
 //
-// bf16 keys scored by a group of two or more query heads take the tensor
-// cores instead: the group's heads times a 16-row tile of keys is a small
-// matrix product, which one warp-level mma per 16 elements of the row
-// computes with fp32 accumulation, so the FMA and widening instructions that
-// make the per-lane form issue-bound disappear (see the consumer below).
+// bf16 keys take the tensor cores instead: the group's query heads times a
+// 16-row tile of keys is a small matrix product (one column per head), which
+// one warp-level mma per 16 elements of the row computes with fp32
+// accumulation.  The FMA and widening instructions that make the per-lane
+// form issue-bound for a GQA group disappear, and the issue slots they free
+// serve the host gather running beside the scoring (see the consumer below).
 #include <math.h>
 
 #include <type_traits>
@@ -63,11 +64,15 @@ struct ScoreGeom {
   static_assert(kStageRows % kGroups == 0, "stage must hold whole row groups");
 };
 
-// Whether a layout is scored on the tensor cores: bf16 keys, a group of two
-// or more query heads, bf16 query.
+// Whether a layout is scored on the tensor cores: bf16 keys and query, and
+// at least DD_SCORE_MMA_MIN_GROUP query heads per KV head (a build option, so
+// that the per-lane form can be measured against it on the same layouts).
+#ifndef DD_SCORE_MMA_MIN_GROUP
+#define DD_SCORE_MMA_MIN_GROUP 1
+#endif
 template <typename T, int G, bool QB>
 __host__ __device__ constexpr bool use_mma() {
-  return std::is_same<T, bf16_t>::value && G >= 2 && !QB;
+  return std::is_same<T, bf16_t>::value && !QB && G >= DD_SCORE_MMA_MIN_GROUP;
 }
 // The tensor-core consumer reads each key row as four lanes' 16-byte pieces.
 // Rows start on 128-byte bank boundaries, so two rows at the same piece meet
@@ -232,7 +237,9 @@ __global__ void __launch_bounds__(kScoreThreads, use_mma<T, G, QB>() && !FUSED ?
     for (int bb = 0; bb < NB; ++bb)
       qb[bb] = gq < G ? ld_ro(q_spec + (size_t)(b * Hq + hk * G + gq) * (D / 8) + 4 * bb + cq)
                       : make_uint4(0u, 0u, 0u, 0u);
-    if (2 * cq < G) head0 = 2 * cq;  // accumulator columns 2c, 2c+1 are heads
+    // Accumulator columns 2c and 2c+1 are heads 2c and 2c+1 (G is 1 or even).
+    if (2 * cq < G) head0 = 2 * cq;
+    constexpr bool kPair = G >= 2;  // does column 2c+1 hold a head as well?
     const int par = gq & 1, hr = gq >> 1;
     // Byte offsets in a stage of the lane's piece of rows g and g+8 of tile 0.
     const int off0 = (par ? HALF * RB + kHalfSkew : 0) + hr * RB + 16 * cq;
@@ -264,18 +271,24 @@ __global__ void __launch_bounds__(kScoreThreads, use_mma<T, G, QB>() && !FUSED ?
         const int j0 = j_begin + t * SR + par * HALF + tau * 8 + hr;  // mma row g
         const int j1 = j0 + 4;                                          // mma row g + 8
         if (j0 < j_end) {
-          const float s0 = acc[0] * scale, s1 = acc[1] * scale;
+          const float s0 = acc[0] * scale;
           lg[j0] = s0;
-          lg[ldn + j0] = s1;
           online_lse(s0, m_run[0], l_run[0]);
-          online_lse(s1, m_run[1], l_run[1]);
+          if (kPair) {
+            const float s1 = acc[1] * scale;
+            lg[ldn + j0] = s1;
+            online_lse(s1, m_run[1], l_run[1]);
+          }
         }
         if (j1 < j_end) {
-          const float s2 = acc[2] * scale, s3 = acc[3] * scale;
+          const float s2 = acc[2] * scale;
           lg[j1] = s2;
-          lg[ldn + j1] = s3;
           online_lse(s2, m_run[0], l_run[0]);
-          online_lse(s3, m_run[1], l_run[1]);
+          if (kPair) {
+            const float s3 = acc[3] * scale;
+            lg[ldn + j1] = s3;
+            online_lse(s3, m_run[1], l_run[1]);
+          }
         }
       }
     }
@@ -406,7 +419,7 @@ __global__ void __launch_bounds__(kScoreThreads, use_mma<T, G, QB>() && !FUSED ?
   for (int g = 0; g < G; ++g) {
     float2 p = make_float2(-INFINITY, 0.f);
     if (head0 >= 0 && g == head0) p = make_float2(m_run[0], l_run[0]);
-    if (MMA && head0 >= 0 && g == head0 + 1) p = make_float2(m_run[1], l_run[1]);
+    if (MMA && G >= 2 && head0 >= 0 && g == head0 + 1) p = make_float2(m_run[1], l_run[1]);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       float2 o;

@@ -1,9 +1,9 @@
 """Every logit of the scoring step against the fp64 oracle, to the fp32
 rounding bound of a d-term dot product.
 
-The scoring kernel has two consumers: bf16 keys scored by a group of two or
-more query heads go through the tensor cores (16-row tiles, each stage filled
-as two halves), everything else through the per-lane form.  The shapes below
+The scoring kernel has two consumers: bf16 keys go through the tensor cores
+(16-row tiles, each stage filled as two halves; one, two, four or eight query
+heads per KV head), fp32 keys through the per-lane form.  The shapes below
 take both, with context lengths whose last stage ends in the first half, in
 the second half, and on a stage boundary, over several chunks per unit.
 
@@ -23,7 +23,7 @@ pytestmark = pytest.mark.gpu
 
 C1, C2 = synth.C1, synth.C2
 CASES = {
-    # tensor-core form (bf16, G >= 2)
+    # tensor-core form (bf16)
     "g4_d128_tail_in_second_half": C2.scaled(batch=2, n_q_heads=8, n_kv_heads=2, ctx_len=3001,
                                              top_k=64, window=0),
     "g4_d128_tail_in_first_half": C2.scaled(batch=1, n_q_heads=8, n_kv_heads=2, ctx_len=2961,
@@ -39,11 +39,19 @@ CASES = {
                                              ctx_len=3001, top_k=64, window=0),
     "g8_d256_tail_in_first_half": C2.scaled(batch=1, n_q_heads=8, n_kv_heads=1, head_dim=256,
                                             ctx_len=2990, top_k=64, window=0),
+    "mha_d128_tail_in_second_half": C2.scaled(batch=2, n_q_heads=2, n_kv_heads=2,
+                                              ctx_len=3001, top_k=64, window=0),
+    "mha_d128_tail_in_first_half": C2.scaled(batch=1, n_q_heads=2, n_kv_heads=2, ctx_len=2961,
+                                             top_k=64, window=0),
+    "mha_d64": C2.scaled(batch=1, n_q_heads=3, n_kv_heads=3, head_dim=64, ctx_len=3050,
+                         top_k=64, window=0),
+    "mha_d256": C2.scaled(batch=1, n_q_heads=2, n_kv_heads=2, head_dim=256, ctx_len=3001,
+                          top_k=64, window=0),
     # per-lane form
-    "mha_bf16_d128": C2.scaled(batch=2, n_q_heads=2, n_kv_heads=2, ctx_len=3001, top_k=64,
-                               window=0),
     "f32_g4_d128": C1.scaled(batch=1, n_q_heads=8, n_kv_heads=2, head_dim=128, ctx_len=2600,
                              top_k=64, window=0),
+    "f32_mha_d64": C1.scaled(batch=2, n_q_heads=2, n_kv_heads=2, ctx_len=3001, top_k=64,
+                             window=0),
 }
 
 
