@@ -18,12 +18,15 @@
 // (max, sum of exp).  All query heads of a GQA group are scored from the same
 // K row.  With FUSED, the unit's last CTA also runs its top-k (select.cuh).
 //
-// bf16 keys take the tensor cores instead: the group's query heads times a
-// 16-row tile of keys is a small matrix product (one column per head), which
-// one warp-level mma per 16 elements of the row computes with fp32
-// accumulation.  The FMA and widening instructions that make the per-lane
-// form issue-bound for a GQA group disappear, and the issue slots they free
-// serve the host gather running beside the scoring (see the consumer below).
+// bf16 keys scored by a group of two or more query heads take the tensor
+// cores instead: the group's heads times a 16-row tile of keys is a small
+// matrix product (one column per head), which one warp-level mma per 16
+// elements of the row computes with fp32 accumulation.  The FMA and widening
+// instructions that make the per-lane form issue-bound for a GQA group
+// disappear, and the issue slots they free serve the host gather running
+// beside the scoring (see the consumer below).  A single head (MHA) keeps the
+// per-lane form, which already streams at the copy rate; the tensor-core form
+// handles it too (build option below) and measured no faster.
 #include <math.h>
 
 #include <type_traits>
@@ -65,10 +68,10 @@ struct ScoreGeom {
 };
 
 // Whether a layout is scored on the tensor cores: bf16 keys and query, and
-// at least DD_SCORE_MMA_MIN_GROUP query heads per KV head (a build option, so
-// that the per-lane form can be measured against it on the same layouts).
+// at least DD_SCORE_MMA_MIN_GROUP query heads per KV head (a build option:
+// 1 sends MHA layers to the tensor cores as well).
 #ifndef DD_SCORE_MMA_MIN_GROUP
-#define DD_SCORE_MMA_MIN_GROUP 1
+#define DD_SCORE_MMA_MIN_GROUP 2
 #endif
 template <typename T, int G, bool QB>
 __host__ __device__ constexpr bool use_mma() {

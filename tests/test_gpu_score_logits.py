@@ -1,11 +1,13 @@
 """Every logit of the scoring step against the fp64 oracle, to the fp32
 rounding bound of a d-term dot product.
 
-The scoring kernel has two consumers: bf16 keys go through the tensor cores
-(16-row tiles, each stage filled as two halves; one, two, four or eight query
-heads per KV head), fp32 keys through the per-lane form.  The shapes below
-take both, with context lengths whose last stage ends in the first half, in
-the second half, and on a stage boundary, over several chunks per unit.
+The scoring kernel has two consumers: bf16 keys scored by two, four or eight
+query heads per KV head go through the tensor cores (16-row tiles, each stage
+filled as two halves), single heads and fp32 keys through the per-lane form
+(a build option sends bf16 single heads to the tensor cores too; these cases
+then cover that).  The shapes below take both, with context lengths whose
+last stage ends in the first half, in the second half, and on a stage
+boundary, over several chunks per unit.
 
 The logits are read from the workspace, whose first region holds them as fp32
 [B][H_q][round_up(n, 4)] (dd_workspace_size).
@@ -39,6 +41,7 @@ CASES = {
                                              ctx_len=3001, top_k=64, window=0),
     "g8_d256_tail_in_first_half": C2.scaled(batch=1, n_q_heads=8, n_kv_heads=1, head_dim=256,
                                             ctx_len=2990, top_k=64, window=0),
+    # per-lane form (bf16, one head per KV head)
     "mha_d128_tail_in_second_half": C2.scaled(batch=2, n_q_heads=2, n_kv_heads=2,
                                               ctx_len=3001, top_k=64, window=0),
     "mha_d128_tail_in_first_half": C2.scaled(batch=1, n_q_heads=2, n_kv_heads=2, ctx_len=2961,
@@ -47,7 +50,7 @@ CASES = {
                          top_k=64, window=0),
     "mha_d256": C2.scaled(batch=1, n_q_heads=2, n_kv_heads=2, head_dim=256, ctx_len=3001,
                           top_k=64, window=0),
-    # per-lane form
+    # per-lane form (fp32 keys)
     "f32_g4_d128": C1.scaled(batch=1, n_q_heads=8, n_kv_heads=2, head_dim=128, ctx_len=2600,
                              top_k=64, window=0),
     "f32_mha_d64": C1.scaled(batch=2, n_q_heads=2, n_kv_heads=2, ctx_len=3001, top_k=64,
