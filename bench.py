@@ -130,15 +130,13 @@ def parse():
 # the half one keeps half the small one's rows in flight on half the SMs: on a
 # store whose gather is bound by address translation, rows in flight beyond
 # what the translations admit only wait, and they hold memory-system slots the
-# scoring beside them needs; the dedicated ones run on a quarter or 40 % of
-# the SMs with so much shared memory (192 KiB) that no scoring CTA shares
-# their SM, and the scoring streams from the others; the load/store gather
-# (eight warps per SM) takes no shared memory.
+# scoring beside them needs; the load/store gather (eight warps per SM) takes
+# no shared memory.  (Gathers on a quarter or 40 % of the SMs with 192 KiB of
+# shared memory each, so that no scoring CTA shares their SMs, were 20-45 %
+# slower per GQA-128K step than the small geometry and are not tried.)
 GATHER_VARIANTS = (("bulk_copy_small", 0, (100, 4096, 3)),
                    ("bulk_copy_wide", 0, (200, 8192, 4)),
                    ("bulk_copy_half", 0, (50, 4096, 3)),
-                   ("bulk_copy_dedicated25", 0, (25, 16384, 6)),
-                   ("bulk_copy_dedicated40", 0, (40, 16384, 6)),
                    ("load_store", 1, (100, 256)))
 
 
