@@ -338,7 +338,9 @@ def config_of(w, args):
             "copy_stream_priority": args.copy_priority,
             "correct_misses": bool(args.correct_misses),
             "landmark_chunk": args.landmarks or None,
-            "topk": "fused into scoring" if args.fused_topk else "separate kernel"}
+            "topk": "fused into scoring" if args.fused_topk else "separate kernel",
+            "scoring": "tensor cores (warp-level mma, fp32 accumulation)"
+                       if getattr(args, "score_tc", False) else "per-lane fp32 FMA"}
 
 
 def run_reference(args, rank, world):
@@ -493,6 +495,7 @@ def run_ours(args, rank, world):
     outs = torch.empty((L, B, Hq, d), dtype=torch.float32, device=dev)
 
     shape = dd.Shape(B, Hq, Hkv, d, n, k, W, w.dtype)
+    args.score_tc = dd.score_tensor_cores(shape) and not args.landmarks
     ctx = dd.Ctx(shape)
     late = bool(args.late_gather) or args.schedule == "late"
     pipe = args.schedule == "pipeline"

@@ -167,6 +167,16 @@ size_t dd_host_page_bytes(void);
 dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes);
 
 /*
+ * How dd_score_topk (and the layer loop) computes this shape's logits: 1 if
+ * on the tensor cores (bf16 keys with at least two query heads per KV head:
+ * warp-level mma on 16-row key tiles, fp32 accumulation), 0 if in the
+ * per-lane form (fp32 FMAs; single heads and fp32 keys).  Both give the
+ * logits within the fp32 rounding bound of a d-term dot product.  Returns
+ * -DD_ERR_INVALID_ARG or -DD_ERR_UNSUPPORTED for a bad shape.
+ */
+int dd_score_tensor_cores(const dd_shape* shape);
+
+/*
  * Steps 1-2 for one layer: logits s[b,h,j] = q_spec[b,h] . K[b,h_kv(h),j] /
  * sqrt(d) for all j < n; lse_out[b,h] = log sum_j exp(s[b,h,j]); selection
  * score a[j] = exp(s_j - lse) (MHA) or sum over the query heads of the group

@@ -120,6 +120,7 @@ def _lib():
                                      ctypes.c_int),
             "dd_host_store_locked": ([ctypes.c_void_p], ctypes.c_int),
             "dd_workspace_size": ([S, ctypes.POINTER(ctypes.c_size_t)], ctypes.c_int),
+            "dd_score_tensor_cores": ([S], ctypes.c_int),
             "dd_set_gather_geometry": ([ctypes.c_int, ctypes.c_int, ctypes.c_int], ctypes.c_int),
             "dd_set_gather_lsu_geometry": ([ctypes.c_int, ctypes.c_int], ctypes.c_int),
             "dd_score_topk": ([S, P, P, P, P, P, P, ctypes.c_size_t, P], ctypes.c_int),
@@ -271,6 +272,14 @@ def workspace_size(shape: Shape) -> int:
     n = ctypes.c_size_t()
     _check(_lib().dd_workspace_size(ctypes.byref(shape.c()), ctypes.byref(n)), "dd_workspace_size")
     return n.value
+
+
+def score_tensor_cores(shape: Shape) -> bool:
+    """Whether this shape's logits are computed on the tensor cores (see dd.h)."""
+    r = _lib().dd_score_tensor_cores(ctypes.byref(shape.c()))
+    if r < 0:
+        _check(-r, "dd_score_tensor_cores")
+    return r == 1
 
 
 def score_topk(shape: Shape, q_spec, k_dev, idx_out, sel_score_out, lse_out, workspace,

@@ -213,6 +213,13 @@ dd_status dd_set_gather_lsu_geometry(int grid_pct, int threads) {
   return set_gather_lsu_geometry(grid_pct, threads);
 }
 
+int dd_score_tensor_cores(const dd_shape* shape) {
+  Dims d;
+  const dd_status st = resolve(shape, &d);
+  if (st != DD_OK) return -(int)st;
+  return score_uses_mma(d.dtype, d.G) ? 1 : 0;
+}
+
 dd_status dd_workspace_size(const dd_shape* shape, size_t* bytes) {
   if (!bytes) return DD_ERR_INVALID_ARG;
   Dims d;

@@ -177,6 +177,10 @@ cudaError_t prepare_kernel(Kernel* fn, unsigned long long* done_mask, int dyn_sm
 // keys per unit (0 if the dtype or head size is unsupported).
 int score_chunk(int dtype, int head_dim, long long units, int n);
 
+// Whether the scoring kernel computes this stored dtype and group size (query
+// heads per KV head) on the tensor cores rather than in the per-lane form.
+bool score_uses_mma(int dtype, int group);
+
 // Read and clear the device-side status words that kernels set when a bounded
 // wait gives up (nonzero: some wait timed out since the last read).
 unsigned int take_score_status();

@@ -515,6 +515,10 @@ int chunk_for(long long units, int n) {
 }
 }  // namespace
 
+bool score_uses_mma(int dtype, int group) {
+  return dtype == DD_BF16 && group >= DD_SCORE_MMA_MIN_GROUP;
+}
+
 int score_chunk(int dtype, int head_dim, long long units, int n) {
   if (dtype == DD_BF16) {
     if (head_dim == 64) return chunk_for<bf16_t, 64>(units, n);

@@ -63,6 +63,21 @@ def test_bad_shapes_rejected(kw, status):
     assert st == status
 
 
+def test_scoring_form_query():
+    """bf16 keys with a GQA group are scored on the tensor cores; one head per
+    KV head and fp32 keys in the per-lane form; bad shapes give the negated
+    status of dd_workspace_size."""
+    for g in (2, 4, 8):
+        assert dd.score_tensor_cores(_shape(n_q_heads=2 * g)) is True
+    assert dd.score_tensor_cores(_shape(n_q_heads=2)) is False
+    assert dd.score_tensor_cores(_shape(head_dim=64, dtype=dd.DD_F32)) is False
+    assert dd.lib().dd_score_tensor_cores(ctypes.byref(_shape(head_dim=96).c())) == \
+        -dd.DD_ERR_UNSUPPORTED
+    with pytest.raises(dd.DDError) as e:
+        dd.score_tensor_cores(_shape(window=4096))
+    assert e.value.status == dd.DD_ERR_INVALID_ARG
+
+
 def test_workspace_size_layout():
     """Logits [B][H_q][round_up(n, 4)] fp32 dominate; the rest is small."""
     for w in (synth.C1, synth.C2, synth.C3, synth.C4, synth.C5):
