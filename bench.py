@@ -338,9 +338,7 @@ def config_of(w, args):
             "copy_stream_priority": args.copy_priority,
             "correct_misses": bool(args.correct_misses),
             "landmark_chunk": args.landmarks or None,
-            "topk": "fused into scoring" if args.fused_topk else "separate kernel",
-            "scoring": "tensor cores (warp-level mma, fp32 accumulation)"
-                       if getattr(args, "score_tc", False) else "per-lane fp32 FMA"}
+            "topk": "fused into scoring" if args.fused_topk else "separate kernel"}
 
 
 def run_reference(args, rank, world):
@@ -936,7 +934,9 @@ def run_ours(args, rank, world):
                      "frac": score_gbs / peak,
                      "traffic": (None if args.profile_case or C
                                  else SCORE_TRAFFIC_BYTES.get((w.name, args.fused_topk))),
-                     "algorithmic_bytes_per_launch": k_bytes},
+                     "algorithmic_bytes_per_launch": k_bytes,
+                     "form": ("tensor cores (warp-level mma, fp32 accumulation)"
+                              if args.score_tc else "per-lane fp32 FMA")},
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": UNIT,
                 "h2d_bytes_per_step": 2 * L * B * Hq * d * elt,
