@@ -454,7 +454,9 @@ def test_full_size_layer_slots_sampled_units(name):
     against the oracle on sampled units (selection, attention, gathered bytes,
     planted keys of every unit), then one decode step whose layers cycle all
     those slots in the layer loop (the benchmark's launch configuration), bit
-    for bit equal to the standalone calls for every layer."""
+    for bit equal to the standalone calls for every layer; the same for the
+    benchmark's default form of the step (pipeline schedule, K and V gathered
+    from one interleaved host store) on the first slot."""
     w = FULL[name]
     slot_ids = full_size_slots(w)
     slots, ref = [], []
@@ -498,6 +500,19 @@ def test_full_size_layer_slots_sampled_units(name):
     ctx.decode_step(_layers(w, slots[:1], fused, 1), compute=compute, copy=copy, fused_topk=True)
     torch.cuda.synchronize()
     assert torch.equal(fused[0], ref[0])
+    # the benchmark's default: pipeline schedule, interleaved [B][H_kv][n][2][d] host store
+    s0 = slots[0]
+    kv0 = dd.host_empty(s0.K_h.shape[:3] + (2,) + s0.K_h.shape[3:], s0.K_h.dtype,
+                        kind="pinned")  # exact size (torch rounds pinned blocks up)
+    kv0[:, :, :, 0, :] = s0.K_h
+    kv0[:, :, :, 1, :] = s0.V_h
+    inter = [torch.full_like(ref[0], float("nan")) for _ in range(2)]
+    ctx.decode_step([dd.LayerIO(s0.q_spec, s0.q, s0.K, None, None, s0.v_win, inter[l],
+                                kv_host=kv0) for l in range(2)],
+                    compute=compute, copy=copy, pipeline=True)
+    torch.cuda.synchronize()
+    for l in range(2):
+        assert torch.equal(inter[l], ref[0]), f"interleaved store, pipeline, layer {l}"
     ctx.close()
-    del slots, ref, outs, fused
+    del slots, ref, outs, fused, kv0, inter, s0
     _free()
