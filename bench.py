@@ -711,6 +711,8 @@ def run_ours(args, rank, world):
         # 3 steps each, twice.
         base = (("overlap", copy, False, False), ("serial", None, False, False),
                 ("pipeline", copy, True, False), ("guarded", copy, False, True))
+        if args.correct_misses:  # the pipeline schedule does not take miss correction
+            base = tuple(b_ for b_ in base if b_[0] != "pipeline")
         variants = GATHER_VARIANTS if args.gather_auto else \
             tuple(v for v in GATHER_VARIANTS if v[1] == args.gather_mode)[:1]
         cands = tuple((name + "+" + vt, cs, pp, gg, vm, vg) for vt, vm, vg in variants
