@@ -188,13 +188,24 @@ def _dev(x) -> Optional[int]:
     return x.data_ptr()
 
 
-def _host(x) -> Optional[int]:
+def _store_bytes(shape: "Shape") -> int:
+    """Bytes of one layer's host K (or V) store [B][H_kv][n][d] for this shape."""
+    elt = 2 if shape.dtype == DD_BF16 else 4
+    return shape.batch * shape.n_kv_heads * shape.ctx_len * shape.head_dim * elt
+
+
+def _host(x, need: Optional[int] = None) -> Optional[int]:
     """Address of a page-locked host buffer (pinned CPU tensor, a tensor from
-    host_empty, or raw int)."""
+    host_empty, or raw int).  With `need`, a tensor must hold at least that
+    many bytes: the GPU reads the store by the shape alone, so a smaller one
+    would be read past its end."""
     if x is None or isinstance(x, int):
         return x
     if x.is_cuda or not x.is_contiguous():
         raise TypeError("expected a contiguous CPU tensor")
+    if need is not None and x.numel() * x.element_size() < need:
+        raise ValueError(f"host store of {x.numel() * x.element_size()} bytes; the shape "
+                         f"reads {need}")
     if not x.is_pinned() and not _lib().dd_host_store_kind(x.data_ptr()):
         raise ValueError("the host KV store must be page-locked (pin_memory=True or host_empty)")
     return x.data_ptr()
@@ -294,14 +305,16 @@ def score_topk(shape: Shape, q_spec, k_dev, idx_out, sel_score_out, lse_out, wor
 
 def gather_h2d(shape: Shape, k_host, v_host, idx, k_buf, v_buf, mode: int = 0, stream=None):
     """Step 3: gather the selected K/V rows from pinned host memory; see dd.h."""
-    _check(_lib().dd_gather_h2d(ctypes.byref(shape.c()), _host(k_host), _host(v_host),
+    nb = _store_bytes(shape)
+    _check(_lib().dd_gather_h2d(ctypes.byref(shape.c()), _host(k_host, nb), _host(v_host, nb),
                                 _dev(idx), _dev(k_buf), _dev(v_buf), mode, _stream(stream)),
            "dd_gather_h2d")
 
 
 def gather_h2d_kv(shape: Shape, kv_host, idx, k_buf, v_buf, mode: int = 0, stream=None):
     """Step 3 from one interleaved host store [B][H_kv][n][2][d]; see dd.h."""
-    _check(_lib().dd_gather_h2d_kv(ctypes.byref(shape.c()), _host(kv_host), _dev(idx),
+    _check(_lib().dd_gather_h2d_kv(ctypes.byref(shape.c()), _host(kv_host, 2 * _store_bytes(shape)),
+                                   _dev(idx),
                                    _dev(k_buf), _dev(v_buf), mode, _stream(stream)),
            "dd_gather_h2d_kv")
 
@@ -326,7 +339,8 @@ def correct_misses(shape: Shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, k_h
         ws_bytes = workspace.numel() * workspace.element_size()
     _check(_lib().dd_correct_misses(
         ctypes.byref(shape.c()), _dev(q), _dev(k_dev), _dev(idx_spec), _dev(k_buf_spec),
-        _dev(v_buf_spec), _host(k_host), _host(v_host), _dev(idx_true_out), _dev(k_buf_out),
+        _dev(v_buf_spec), _host(k_host, _store_bytes(shape)), _host(v_host, _store_bytes(shape)),
+        _dev(idx_true_out), _dev(k_buf_out),
         _dev(v_buf_out), _dev(miss_out), _dev(mass_out), _dev(workspace), ws_bytes,
         _stream(stream)), "dd_correct_misses")
 
@@ -340,7 +354,8 @@ def correct_misses_kv(shape: Shape, q, k_dev, idx_spec, k_buf_spec, v_buf_spec, 
         ws_bytes = workspace.numel() * workspace.element_size()
     _check(_lib().dd_correct_misses_kv(
         ctypes.byref(shape.c()), _dev(q), _dev(k_dev), _dev(idx_spec), _dev(k_buf_spec),
-        _dev(v_buf_spec), _host(kv_host), _dev(idx_true_out), _dev(k_buf_out),
+        _dev(v_buf_spec), _host(kv_host, 2 * _store_bytes(shape)), _dev(idx_true_out),
+        _dev(k_buf_out),
         _dev(v_buf_out), _dev(miss_out), _dev(mass_out), _dev(workspace), ws_bytes,
         _stream(stream)), "dd_correct_misses_kv")
 
@@ -429,13 +444,16 @@ class Ctx:
             pass
 
     @staticmethod
-    def pack(layers: Sequence[LayerIO]):
-        """Marshal the per-layer buffers once (reuse across steps)."""
+    def pack(layers: Sequence[LayerIO], shape: Optional[Shape] = None):
+        """Marshal the per-layer buffers once (reuse across steps).  With the
+        shape, host stores smaller than it reads are refused."""
         arr = (dd_layer_io * len(layers))()
+        nb = None if shape is None else _store_bytes(shape)
         for i, io in enumerate(layers):
-            arr[i] = dd_layer_io(_dev(io.q_spec), _dev(io.q), _dev(io.k_dev), _host(io.k_host),
-                                 _host(io.v_host), _dev(io.v_win), _dev(io.out),
-                                 _dev(io.landmarks), _dev(io.k_win), _host(io.kv_host))
+            arr[i] = dd_layer_io(_dev(io.q_spec), _dev(io.q), _dev(io.k_dev),
+                                 _host(io.k_host, nb), _host(io.v_host, nb), _dev(io.v_win),
+                                 _dev(io.out), _dev(io.landmarks), _dev(io.k_win),
+                                 _host(io.kv_host, None if nb is None else 2 * nb))
         return arr
 
     def set_landmark_chunk(self, chunk: int):
@@ -447,7 +465,7 @@ class Ctx:
                     correct_misses: bool = False, landmarks: bool = False,
                     fused_topk: bool = False, debug_delay: str = "", guarded: bool = False):
         """Enqueue one decode step over the layers (LayerIO list or a packed array)."""
-        arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
+        arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers, self.shape)
         cs = _stream(compute)
         xs = None if copy is None else _stream(copy)
         # timing: False, True (every phase) or "light" (step and scoring only)
@@ -475,7 +493,7 @@ class Ctx:
         """Capture one decode step into a CUDA graph held by the context (the
         step runs once directly first); replay it with replay_step.  `compute`
         must be a created stream (capture is not possible on the default one)."""
-        arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers)
+        arr = layers if isinstance(layers, ctypes.Array) else self.pack(layers, self.shape)
         _check(_lib().dd_ctx_capture_step(self._h, arr, len(arr), _stream(compute),
                                           None if copy is None else _stream(copy),
                                           self._flags(**schedule)), "dd_ctx_capture_step")

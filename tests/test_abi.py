@@ -170,9 +170,35 @@ def test_timing_calls_reject_null_context():
 def test_pageable_host_store_rejected_by_binding():
     import torch
     shp = _shape()
-    t = torch.empty(16, dtype=torch.bfloat16)
-    with pytest.raises(ValueError):
-        dd.gather_h2d(shp, t, t, 16, 16, 16)
+    full = torch.empty((2, 2, 4096, 128), dtype=torch.bfloat16)  # the shape's size, pageable
+    with pytest.raises(ValueError, match="page-locked"):
+        dd.gather_h2d(shp, full, full, 16, 16, 16)
+    kv = torch.empty((2, 2, 4096, 2, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="page-locked"):
+        dd.gather_h2d_kv(shp, kv, 16, 16, 16)
+
+
+def test_host_store_smaller_than_the_shape_rejected_by_binding():
+    """The GPU reads a host store by the shape alone, so the binding refuses
+    one with fewer bytes than the shape reads, before anything is launched."""
+    import torch
+    shp = _shape()
+    small = torch.empty((2, 2, 4095, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="the shape reads"):
+        dd.gather_h2d(shp, small, small, 16, 16, 16)
+    one_tensor = torch.empty((2, 2, 4096, 128), dtype=torch.bfloat16)  # K only, not K and V
+    with pytest.raises(ValueError, match="the shape reads"):
+        dd.gather_h2d_kv(shp, one_tensor, 16, 16, 16)
+    with pytest.raises(ValueError, match="the shape reads"):
+        dd.correct_misses(shp, 16, 16, 16, 16, 16, small, small, 16, 16, 16, 16, 16, 16,
+                          ws_bytes=1)
+    with pytest.raises(ValueError, match="the shape reads"):
+        dd.correct_misses_kv(shp, 16, 16, 16, 16, 16, one_tensor, 16, 16, 16, 16, 16, 16,
+                             ws_bytes=1)
+    io = dd.LayerIO(16, 16, 16, None, None, None, 16, kv_host=one_tensor)
+    with pytest.raises(ValueError, match="the shape reads"):
+        dd.Ctx.pack([io], shp)
+    dd.Ctx.pack([io._replace(kv_host=None, k_host=16, v_host=16)], shp)  # raw addresses pass
 
 
 def test_product_path_never_touches_the_oracle():
