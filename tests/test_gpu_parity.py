@@ -497,6 +497,7 @@ def test_full_size_layer_slots_sampled_units(name):
         assert torch.equal(outs[l], ref[l % len(slots)]), f"layer {l} (slot {slot_ids[l % len(slots)]})"
     # the fused form of steps 1-2 (its last-CTA selection samples at these sizes too)
     fused = [torch.full_like(ref[0], float("nan"))]
+    compute.wait_stream(torch.cuda.current_stream())
     ctx.decode_step(_layers(w, slots[:1], fused, 1), compute=compute, copy=copy, fused_topk=True)
     torch.cuda.synchronize()
     assert torch.equal(fused[0], ref[0])
@@ -507,12 +508,16 @@ def test_full_size_layer_slots_sampled_units(name):
     kv0[:, :, :, 0, :] = s0.K_h
     kv0[:, :, :, 1, :] = s0.V_h
     inter = [torch.full_like(ref[0], float("nan")) for _ in range(2)]
+    compute.wait_stream(torch.cuda.current_stream())  # the NaN fills come first
     ctx.decode_step([dd.LayerIO(s0.q_spec, s0.q, s0.K, None, None, s0.v_win, inter[l],
                                 kv_host=kv0) for l in range(2)],
                     compute=compute, copy=copy, pipeline=True)
     torch.cuda.synchronize()
     for l in range(2):
-        assert torch.equal(inter[l], ref[0]), f"interleaved store, pipeline, layer {l}"
+        bad = (inter[l] != ref[0]).flatten(1).any(1).nonzero().flatten().tolist()
+        assert not bad, (f"interleaved store, pipeline, layer {l}: requests {bad[:8]} differ; "
+                         f"NaN {int(inter[l].isnan().sum())}, max |diff| "
+                         f"{float((inter[l] - ref[0]).abs().nan_to_num(0).max()):.3g}")
     ctx.close()
     del slots, ref, outs, fused, kv0, inter, s0
     _free()
